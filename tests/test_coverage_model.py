@@ -1,0 +1,142 @@
+"""Pins for the tile-coverage model and the raster map (no GPU)."""
+import json
+import math
+import os
+import random
+
+import pytest
+
+from oracle import coverage as cv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tail_example.json")
+
+
+def test_worked_tail_example_static_6t():
+    g = json.load(open(GOLDEN))
+    st = g["static"]
+    s = cv.simulate(g["n_tiles"], cv.STATIC, resident=st["resident"], n_workers=st["planned_workers"])
+    cv.check_schedule(s)
+    assert s.makespan == st["makespan_t"]
+    assert {str(w): seq for w, seq in s.sequences.items()} == st["sequences"]
+
+
+def test_worked_tail_example_clc_4t():
+    g = json.load(open(GOLDEN))
+    c = g["clc"]
+    for prefetch in (False, True):
+        s = cv.simulate(g["n_tiles"], cv.CLC, resident=c["resident"], prefetch=prefetch)
+        cv.check_schedule(s)
+        assert s.makespan == c["makespan_t"]
+        assert sorted(len(v) for v in s.sequences.values()) == [c["tiles_per_worker"]] * c["resident"]
+
+
+def test_nonpersistent_also_balances_the_example():
+    # The page notes the plain non-persistent grid also spreads the 12 blocks dynamically.
+    s = cv.simulate(12, cv.NONPERSISTENT, resident=3)
+    cv.check_schedule(s)
+    assert s.makespan == 4
+    assert s.owner == list(range(12))
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 12, 147, 148, 149, 296, 297])
+@pytest.mark.parametrize("R", [1, 3, 148])
+def test_unit_cost_closed_forms(T, R):
+    clc = cv.simulate(T, cv.CLC, resident=R)
+    cv.check_schedule(clc)
+    assert clc.makespan == math.ceil(T / R)
+    npers = cv.simulate(T, cv.NONPERSISTENT, resident=R)
+    assert npers.makespan == math.ceil(T / R)
+    W = 148
+    st = cv.simulate(T, cv.STATIC, resident=R, n_workers=W)
+    cv.check_schedule(st)
+    per_worker = math.ceil(T / W)
+    busy = min(W, T)
+    # workers run in waves of R slots, each wave as long as its longest worker
+    waves = math.ceil(busy / R)
+    if busy <= R:
+        assert st.makespan == per_worker
+    else:
+        assert per_worker <= st.makespan <= waves * per_worker
+    assert st.owner == cv.expected_owner_static(T, W)
+
+
+def test_static_planned_above_resident_tail():
+    # 74 planned clusters on 62 resident, 4096 unit tiles: workers 0..25 own 56 tiles,
+    # 26..73 own 55.  The 55-tile workers among the first 62 free their slots at 55,
+    # and the 12 late workers (55 tiles each) then run to 110.
+    st = cv.simulate(4096, cv.STATIC, resident=62, n_workers=74)
+    assert st.makespan == 110
+    clc = cv.simulate(4096, cv.CLC, resident=62)
+    assert clc.makespan == math.ceil(4096 / 62)
+
+
+@pytest.mark.parametrize("T,R", [(1, 1), (3, 2), (5, 2), (6, 3), (7, 3), (7, 2)])
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_exhaustive_cancel_orders_keep_coverage(T, R, prefetch):
+    n = 0
+    for s in cv.enumerate_clc_orders(T, R, prefetch=prefetch):
+        cv.check_schedule(s)
+        n += 1
+    assert n >= 1
+
+
+def test_exhaustive_with_uneven_costs():
+    rng = random.Random(5)
+    for _ in range(20):
+        T = rng.randint(1, 6)
+        R = rng.randint(1, 3)
+        cost = [rng.choice([0.5, 1.0, 2.0, 3.0]) for _ in range(T)]
+        for s in cv.enumerate_clc_orders(T, R, cost=cost):
+            cv.check_schedule(s)
+            assert s.makespan >= max(cost)
+
+
+def test_planted_double_claim_is_caught():
+    s = cv.simulate(6, cv.CLC, resident=2)
+    s.claims[3] = 2
+    with pytest.raises(AssertionError):
+        cv.check_schedule(s)
+
+
+@pytest.mark.parametrize("mt,nt,G", [(1, 1, 8), (3, 4, 8), (24, 32, 8), (17, 5, 8), (5, 7, 1), (9, 3, 4), (64, 32, 8)])
+def test_raster_is_a_bijection(mt, nt, G):
+    seen = {cv.raster(c, mt, nt, G) for c in range(mt * nt)}
+    assert seen == {(m, n) for m in range(mt) for n in range(nt)}
+
+
+def test_raster_closed_forms():
+    mt, nt = 6, 5
+    # one band covering all rows: column-major order
+    assert [cv.raster(c, mt, nt, 8) for c in range(mt * nt)] == [(c % mt, c // mt) for c in range(mt * nt)]
+    # band height 1: row-major order
+    assert [cv.raster(c, mt, nt, 1) for c in range(mt * nt)] == [(c // nt, c % nt) for c in range(mt * nt)]
+    # 17 rows in bands of 8: the last band has one row, walked along n
+    assert [cv.raster(16 * 5 + j, 17, 5, 8) for j in range(5)] == [(16, j) for j in range(5)]
+    assert cv.raster(1, 17, 5, 8) == (1, 0) and cv.raster(8, 17, 5, 8) == (0, 1)
+
+
+def test_grouped_tile_offsets():
+    tiles_m = [1, 3, 2]
+    nt = 2
+    out = [cv.grouped_tile(c, tiles_m, nt) for c in range(12)]
+    assert out[0] == (0, 0, 0) and out[1] == (0, 0, 1)
+    assert out[2] == (1, 0, 0) and out[3] == (1, 1, 0) and out[5] == (1, 0, 1)
+    assert out[8] == (2, 0, 0) and out[11] == (2, 1, 1)
+    with pytest.raises(ValueError):
+        cv.grouped_tile(12, tiles_m, nt)
+
+
+def test_device_log_checker_accepts_and_rejects():
+    T, W = 10, 4
+    owner = cv.expected_owner_static(T, W)
+    cv.check_device_log(cv.STATIC, owner, [1] * T, [0, 1, 2, 3], W, n_workers=W)
+    with pytest.raises(AssertionError):
+        cv.check_device_log(cv.STATIC, owner, [1] * 9 + [0], [0, 1, 2, 3], W, n_workers=W)
+    # CLC: launches 0..2 ran, 3..5 were stolen
+    owner = [0, 1, 2, 0, 1, 2]
+    first = [0, 1, 2, -1, -1, -1]
+    cv.check_device_log(cv.CLC, owner, [1] * 6, first, 6)
+    with pytest.raises(AssertionError):   # launch 3 ran although tile 3 was stolen by 0
+        cv.check_device_log(cv.CLC, [0, 1, 2, 0, 3, 2], [1] * 6, [0, 1, 2, 3, -1, -1], 6)
+    with pytest.raises(AssertionError):   # a worker did not start with its own tile
+        cv.check_device_log(cv.CLC, owner, [1] * 6, [0, 1, 3, -1, -1, -1], 6)
