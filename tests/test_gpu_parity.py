@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element,
+and the device ownership log against the coverage model (bit-exact invariants)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from oracle import coverage as cv
+from tests.gpu_helpers import TILE_128, TILE_256, assert_close, check_log, cluster_rows, run
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["clc", "static", "nonpersistent"]
+SHAPES = [(TILE_256, 1), (TILE_128, 1), (TILE_256, 2)]
+SHAPE_IDS = ["n256c1", "n128c1", "n256c2"]
+
+
+@pytest.fixture(scope="module")
+def g():
+    import blackwell_clc_dynamic_gb300 as m
+    h = m.Gemm(0)
+    yield h
+    h.close()
+
+
+def test_tiny_config_clc(g):
+    """384x512x256, 128x128 tiles, 12 tiles, CLC over a grid of 12 CTAs."""
+    w = wl.TINY
+    A, B = wl.make_inputs(w)
+    C = run(g, A, B, tile=TILE_128, cluster=1, sched="clc")
+    assert_close(C, oracle.gemm(A, B))
+    info = g.last_launch()
+    assert info["grid_ctas"] == 12 and info["n_tiles"] == 12
+    owner, claims, first = g.get_log()
+    assert claims.tolist() == [1] * 12
+    check_log(g, "clc", [3], 4, 1)
+
+
+@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("mode", MODES)
+def test_integer_inputs_bit_exact(g, tile, cl, mode):
+    """Integer entries in [-4, 4]: every fp32 partial sum is an exact integer below 2^24,
+    so any accumulation order must reproduce the oracle bit for bit."""
+    M, N, K = 512, 768, 1024
+    A = wl.make_matrix((M, K), 11, "int")
+    B = wl.make_matrix((K, N), 12, "int")
+    C = run(g, A, B, tile=tile, cluster=cl, sched=mode, num_workers=7)
+    ref = oracle.gemm(A, B)
+    assert np.array_equal(C.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("mode", MODES)
+def test_uniform_ragged_tail(g, tile, cl, mode):
+    """Several tiles in each direction plus ragged M, N and K edges."""
+    M, N, K = 1000, 776, 1000
+    A = wl.make_matrix((M, K), 21)
+    B = wl.make_matrix((K, N), 22)
+    C = run(g, A, B, tile=tile, cluster=cl, sched=mode, num_workers=5)
+    assert_close(C, oracle.gemm(A, B))
+    mt = cluster_rows(M, cl)
+    nt = math.ceil(N / tile[1])
+    check_log(g, mode, [mt], nt, cl, num_workers=5 if mode == "static" else None)
+
+
+def test_identity_and_rank_one(g):
+    K = 256
+    A = wl.make_matrix((384, K), 31)
+    eye = torch.zeros((K, 512), dtype=torch.bfloat16)
+    eye[torch.arange(K), torch.arange(K)] = 1
+    C = run(g, A, eye)
+    assert np.array_equal(C[:, :K], A.float().numpy()) and np.all(C[:, K:] == 0)
+    u = torch.tensor([2.0 ** (i % 7 - 3) * (-1) ** i for i in range(256)])
+    v = torch.tensor([2.0 ** (j % 5 - 2) * (-1) ** (j // 3) for j in range(512)])
+    A1 = u[:, None].expand(256, K).contiguous().to(torch.bfloat16)
+    B1 = v[None, :].expand(K, 512).contiguous().to(torch.bfloat16)
+    C1 = run(g, A1, B1, sched="static")
+    assert np.array_equal(C1.astype(np.float64), K * np.outer(u.double().numpy(), v.double().numpy()))
+
+
+def test_empty_and_degenerate(g):
+    # M == 0: nothing launched, no error
+    A = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((0, 256), dtype=torch.float32, device="cuda")
+    g.run(A, B, C)
+    g.sync()
+    assert g.last_launch()["launched"] == 0
+    # K == 0: C = 0
+    A = torch.zeros((200, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((200, 256), float("nan"), device="cuda")
+    g.run(A, B, C)
+    g.sync()
+    assert torch.all(C == 0)
+    # a single tile, single row / column block
+    A = wl.make_matrix((1, 64), 41)
+    B = wl.make_matrix((64, 8), 42)
+    assert_close(run(g, A, B), oracle.gemm(A, B))
+
+
+def test_argument_errors(g):
+    import blackwell_clc_dynamic_gb300 as m
+    A = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((128, 256), dtype=torch.float32, device="cuda")
+    h = g.h
+    assert m.gemm_run(h, 128, 256, 64, A, B, C, tile=(128, 192, 64)) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run(h, 128, 256, 64, A, B, C, tile=(128, 128, 64), cluster=2) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run(h, 128, 256, 64, A, B, C, sched=7) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run(h, 128, 256, 60, A, B, C) == m.GEMM_ERR_ALIGNMENT
+    assert m.gemm_run(h, 128, 252, 64, A, B, C) == m.GEMM_ERR_ALIGNMENT
+    assert m.gemm_run(h, 128, 256, 64, A.data_ptr() + 2, B, C) == m.GEMM_ERR_ALIGNMENT
+    assert m.gemm_run(h, -1, 256, 64, A, B, C) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run(h, 128, 256, 64, None, B, C) == m.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T", [1, 2, 5])
+def test_static_owner_map_exact(g, T):
+    """Static: tile t is run by worker t mod W, bit-exact; W above the tile count too."""
+    M, N, K = 128 * 3 * T, 512, 128
+    A = wl.make_matrix((M, K), 51)
+    B = wl.make_matrix((K, N), 52)
+    for W in (1, 4, 148):
+        C = run(g, A, B, sched="static", num_workers=W)
+        assert_close(C, oracle.gemm(A, B))
+        owner_lin, first = check_log(g, "static", [3 * T], 2, 1, num_workers=W)
+        assert owner_lin == cv.expected_owner_static(6 * T, W)
+
+
+@pytest.mark.parametrize("n_fetch", [0, 1, 5])
+def test_clc_injected_failure_keeps_coverage(g, n_fetch):
+    """After n successful fetches the scheduler reports a failed fetch without issuing a
+    cancel; the workers stop and the launches nobody took run normally."""
+    g.set_opts(inject_fail_after=n_fetch)
+    try:
+        M, N, K = 128 * 40, 512, 256
+        A = wl.make_matrix((M, K), 61)
+        B = wl.make_matrix((K, N), 62)
+        C = run(g, A, B, sched="clc")
+        assert_close(C, oracle.gemm(A, B))
+        owner_lin, first = check_log(g, "clc", [40], 2, 1)
+        counts = np.bincount(np.array(owner_lin), minlength=80)
+        assert counts.max() <= n_fetch + 1
+    finally:
+        g.set_opts(inject_fail_after=-1)
+
+
+@pytest.mark.parametrize("T", [147, 148, 149, 296, 297])
+def test_tail_sweep_sampled(g, T):
+    """Tail sweep workload (M = 128 T, N = 256, K = 8192, seed 2), CLC and static-persistent:
+    the first and last tile in full plus 512 scattered elements against the oracle."""
+    w = wl.tail(T)
+    A, B = wl.make_inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    rng = np.random.default_rng(T)
+    rows = rng.integers(0, w.M, 512)
+    cols = rng.integers(0, w.N, 512)
+    ref_e = oracle.gemm_entries(A, B, rows, cols)
+    ref_first = oracle.gemm_block(A, B, 0, 128, 0, 256)
+    ref_last = oracle.gemm_block(A, B, w.M - 128, w.M, 0, 256)
+    for mode in ("clc", "static"):
+        C = torch.full((w.M, w.N), float("nan"), device="cuda")
+        g.run(dA, dB, C, sched=mode, num_workers=148)
+        g.sync()
+        Ch = C.cpu().numpy()
+        assert_close(Ch[rows, cols], ref_e)
+        assert_close(Ch[:128], ref_first)
+        assert_close(Ch[-128:], ref_last)
+        assert not np.isnan(Ch).any()
+        check_log(g, mode, [T], 1, 1, num_workers=148 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+def test_grouped_small(g, tile, cl):
+    """Grouped flat grid over problems of uneven height (including an empty one)."""
+    Ms = [128, 300, 0, 1024, 64]
+    N, K = 512, 384
+    gen = torch.Generator().manual_seed(71)
+    As = [(torch.rand((m, K), generator=gen) * 2 - 1).to(torch.bfloat16) for m in Ms]
+    Bs = [(torch.rand((K, N), generator=gen) * 2 - 1).to(torch.bfloat16) for _ in Ms]
+    if True:
+        for mode in MODES:
+            dA = [a.cuda() for a in As]
+            dB = [b.cuda() for b in Bs]
+            dC = [torch.full((m, N), float("nan"), device="cuda") for m in Ms]
+            g.run_grouped(dA, dB, dC, tile=tile, cluster=cl, sched=mode, num_workers=3)
+            g.sync()
+            for a, b, c in zip(As, Bs, dC):
+                if a.shape[0]:
+                    assert_close(c.cpu().numpy(), oracle.gemm(a, b))
+            tiles_m = [math.ceil(m / (128 * cl)) for m in Ms]
+            check_log(g, mode, tiles_m, math.ceil(N / tile[1]), cl, num_workers=3 if mode == "static" else None)
+
+
+def test_run_host_matches_device_run(g):
+    A = wl.make_matrix((640, 512), 81)
+    B = wl.make_matrix((512, 768), 82)
+    Ch = torch.empty((640, 768), dtype=torch.float32).pin_memory()
+    g.run_host(A.pin_memory(), B.pin_memory(), Ch)
+    g.sync()
+    assert_close(Ch.numpy(), oracle.gemm(A, B))
