@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s & % of bf16 dense peak (CLC vs static vs non-persistent) at 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh", "launch.cuh", "api.cu"]
+# files whose change invalidates the committed DRAM-traffic counters
+KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh", "launch.cuh", "kern_n128_c1.cu", "kern_n256_c1.cu", "kern_n256_c2.cu"]
 
 
 def parse():
@@ -73,9 +74,8 @@ def load_peaks():
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blackwell_clc_dynamic_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
