@@ -27,6 +27,7 @@ GEMM_ERR_OOM = -6
 GEMM_ERR_CUDA = -7
 GEMM_ERR_NO_DEVICE = -8
 GEMM_ERR_TOO_LARGE = -9
+GEMM_ERR_SCRATCH_LIMIT = -10
 
 GEMM_SCHED_CLC = 0
 GEMM_SCHED_STATIC = 1
@@ -38,7 +39,7 @@ EXPORTS = (
     "gemm_opts_default", "gemm_create", "gemm_destroy", "gemm_set_opts", "gemm_run", "gemm_run_grouped",
     "gemm_run_host", "gemm_sync", "gemm_device_error", "gemm_last_launch", "gemm_get_log", "gemm_get_trace",
     "gemm_max_active_clusters", "gemm_sm_count", "gemm_occupy_start", "gemm_occupy_wait_resident",
-    "gemm_occupy_stop", "gemm_strerror", "gemm_version",
+    "gemm_occupy_stop", "gemm_strerror", "gemm_version", "gemm_run_noalloc",
 )
 
 
@@ -94,6 +95,7 @@ def _load() -> ctypes.CDLL:
         "gemm_occupy_stop": (i32, [H, ctypes.POINTER(i32)]),
         "gemm_strerror": (ctypes.c_char_p, [i32]),
         "gemm_version": (i32, []),
+        "gemm_run_noalloc": (i32, [i64, i64, i64, p, p, p, gemm_tile_t, gemm_cluster_t, i32, i32, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -197,6 +199,14 @@ def gemm_run_grouped(h, M_g: Sequence[int], N, K, A_g, B_g, C_g, tile=(128, 256,
     b = (ctypes.c_void_p * G)(*[_ptr(x) for x in B_g])
     c = (ctypes.c_void_p * G)(*[_ptr(x) for x in C_g])
     return lib.gemm_run_grouped(h, G, m, N, K, a, b, c, _tile(tile), _cluster(cluster), _sched(sched),
+                                num_workers, _stream(stream))
+
+
+def gemm_run_noalloc(M, N, K, A, B, C, tile=(128, 256, 64), cluster=1, sched="clc", num_workers=0,
+                     stream=None) -> int:
+    """gemm_run without a handle and without any device allocation (fixed scratch; see the
+    C header for its limits and sharing rules)."""
+    return lib.gemm_run_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), _tile(tile), _cluster(cluster), _sched(sched),
                                 num_workers, _stream(stream))
 
 

@@ -1,0 +1,184 @@
+// gemm_run_noalloc: the GEMM of gemm_run for callers that cannot allocate device memory.
+//
+// Some callers can't call cudaMalloc: a process whose device memory is handed entirely
+// to its own pool allocator or held under a hard cap, or a latency-critical path where a
+// cudaMalloc (which may synchronise the device) is not acceptable.  gemm_run needs a
+// handle whose workspace (error word, ownership log) is allocated with cudaMalloc; this
+// entry point instead keeps that scratch in one fixed, file-scope device array that
+// every GPU which loads the library holds until the process exits.  The caller still
+// passes A, B and C.
+//
+// Limits and sharing:
+//   - at most kNoAllocMaxTiles CTA tiles and kNoAllocMaxWorkers launched workers per
+//     call; larger problems are rejected with GEMM_ERR_SCRATCH_LIMIT before anything is
+//     launched;
+//   - every call on a device uses the same array and leaves its contents behind; each
+//     call clears the parts that must start at zero (error word, claim counts) on its
+//     stream before its kernel.  Calls that overlap on the GPU (other streams, other
+//     threads) race on the array: serialise them.
+//   - the first call on a device (with that device current) looks up the array's
+//     device address with cudaGetSymbolAddress; make that first call before any stream
+//     capture begins.
+//   - nothing here calls cudaMalloc, cudaFree or an allocating library routine.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "clcgemm.h"
+#include "launch.cuh"
+
+using namespace clcg;
+
+namespace {
+
+constexpr int64_t kNoAllocMaxTiles = 65536;     // CTA tiles (ownership-log entries)
+constexpr int64_t kNoAllocMaxWorkers = 65536;   // launched workers (first-tile entries)
+constexpr int64_t kErrWords = 4;
+constexpr int64_t kScratchWords = kErrWords + 2 * kNoAllocMaxTiles + kNoAllocMaxWorkers;   // 768 KiB + 16 B
+
+// [0, 4) error word | owner[kNoAllocMaxTiles] | claims[kNoAllocMaxTiles] | first[kNoAllocMaxWorkers]
+static __device__ __align__(256) int32_t g_noalloc_scratch[kScratchWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int32_t* g_scratch_dev[kMaxDevices];   // device address of g_noalloc_scratch, per device
+int g_sms[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return GEMM_OK;
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver || e == cudaErrorInitializationError)
+    return GEMM_ERR_NO_DEVICE;
+  return GEMM_ERR_CUDA;
+}
+
+// Once per device, with that device current: resolve the scratch array's device address.
+int setup_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_INVALID_ARG;
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return GEMM_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (g_scratch_dev[dev]) return GEMM_OK;
+  int major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) return from_cuda(e == cudaSuccess ? cudaErrorUnknown : e);
+  g_scratch_dev[dev] = static_cast<int32_t*>(p);
+  g_sms[dev] = sms;
+  return GEMM_OK;
+}
+
+int encode(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, float* C,
+                                gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched, int num_workers,
+                                void* stream) {
+  // argument rules of gemm_run
+  if (M < 0 || N < 0 || K < 0 || num_workers < 0) return GEMM_ERR_INVALID_ARG;
+  if (sched != GEMM_SCHED_CLC && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_NONPERSISTENT)
+    return GEMM_ERR_INVALID_ARG;
+  if (tile.bm != 128 || tile.bk != 64 || cluster.y != 1 || cluster.z != 1) return GEMM_ERR_INVALID_ARG;
+  int bn = 0, cl = 0;
+  if (cluster.x == 1 && (tile.bn == 128 || tile.bn == 256)) {
+    bn = tile.bn;
+    cl = 1;
+  } else if (cluster.x == 2 && tile.bn == 256) {
+    bn = 256;
+    cl = 2;
+  } else {
+    return GEMM_ERR_INVALID_ARG;
+  }
+  if ((K % 8) != 0 || (N % 8) != 0) return GEMM_ERR_ALIGNMENT;
+  if (M > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX) return GEMM_ERR_TOO_LARGE;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(C) || (K > 0 && (misaligned(A) || misaligned(B)))) return GEMM_ERR_ALIGNMENT;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  int rc = setup_device(dev);
+  if (rc) return rc;
+
+  const int64_t mt = (M + (int64_t)BM * cl - 1) / ((int64_t)BM * cl);
+  const int64_t nt = (N + bn - 1) / bn;
+  const int64_t total = mt * nt;
+  const int64_t n_tiles = total * cl;
+  int64_t workers = total;
+  if (sched == GEMM_SCHED_STATIC) {
+    workers = num_workers > 0 ? num_workers : (g_sms[dev] / cl > 0 ? g_sms[dev] / cl : 1);
+  }
+  if (n_tiles > kNoAllocMaxTiles || workers > kNoAllocMaxWorkers) return GEMM_ERR_SCRATCH_LIMIT;
+
+  int32_t* err = g_scratch_dev[dev];
+  int32_t* owner = err + kErrWords;
+  int32_t* claims = owner + kNoAllocMaxTiles;
+  int32_t* first = claims + kNoAllocMaxTiles;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(err, 0, kErrWords * sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(owner, 0xFF, (size_t)n_tiles * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(claims, 0, (size_t)n_tiles * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(first, 0xFF, (size_t)workers * 4, s);
+  if (e != cudaSuccess) return from_cuda(e);
+
+  Params p;
+  memset(&p, 0, sizeof p);
+  if (K > 0) {
+    rc = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, BM);
+    if (rc) return rc;
+    rc = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64, BK);
+    if (rc) return rc;
+  }
+  rc = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 4, EPI_CHUNK, 32);
+  if (rc) return rc;
+  p.G = 0;
+  p.mt = (int)mt;
+  p.nt = (int)nt;
+  p.total = (int)total;
+  p.k_blocks = (int)((K + BK - 1) / BK);
+  p.raster_group = 8;
+  p.log_owner = owner;
+  p.log_claims = claims;
+  p.log_first = first;
+  p.trace = nullptr;
+  p.err = err;
+  p.timeout_ns = 2000000000LL;
+  p.inject_fail_after = -1;
+
+  const int grid = (int)(workers * cl);
+  if (cl == 2) e = launch_n256_c2((int)sched, p, grid, s);
+  else if (bn == 128) e = launch_n128_c1((int)sched, p, grid, s);
+  else e = launch_n256_c1((int)sched, p, grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}

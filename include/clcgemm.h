@@ -54,6 +54,7 @@ extern "C" {
 #define GEMM_ERR_CUDA                -7  /* another CUDA runtime / driver error */
 #define GEMM_ERR_NO_DEVICE           -8  /* no CUDA device / driver in this process */
 #define GEMM_ERR_TOO_LARGE           -9  /* a tile or worker count exceeds 2^31 - 1 */
+#define GEMM_ERR_SCRATCH_LIMIT      -10  /* gemm_run_noalloc: more tiles or workers than its fixed scratch holds */
 
 /* ---------------------------------------------------------------- types */
 typedef struct gemm_handle *gemm_handle_t;
@@ -197,6 +198,31 @@ CLCGEMM_API int gemm_sm_count(gemm_handle_t h, int *sms);
 CLCGEMM_API int gemm_occupy_start(gemm_handle_t h, int n_ctas, int64_t limit_ns, void *stream);
 CLCGEMM_API int gemm_occupy_wait_resident(gemm_handle_t h, int wait_ms);
 CLCGEMM_API int gemm_occupy_stop(gemm_handle_t h, int *status);
+
+/* ---------------------------------------------------------------- no-allocation variant */
+
+/* gemm_run_noalloc: the product of gemm_run, for callers that cannot allocate device
+ * memory (a process whose device memory belongs to its own pool allocator or sits under
+ * a hard cap, or a latency-critical path that cannot afford a cudaMalloc).  The paper
+ * has no counterpart: this is a deployment convenience, not part of the method.
+ *   - No handle: it runs on the current device with the default options (ownership log
+ *     on, 2 s wait bound, raster band 8).  Same arguments and shape rules as gemm_run.
+ *   - Its scratch (device error word and ownership log) is one fixed file-scope device
+ *     array of 768 KiB + 16 B, held by every GPU that loads the library until the process
+ *     exits.  At most 65536 CTA tiles and 65536 launched workers per call; larger
+ *     problems return GEMM_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *   - The first call on a device (that device current) resolves the array's address;
+ *     make that first call before any stream capture begins.
+ *   - All calls share the array: each clears what must start at zero on its own stream,
+ *     but calls that overlap on the GPU (different streams or threads) race.  The log
+ *     and error word it writes are not read back by any entry point; device-side wait
+ *     timeouts are therefore not reported.
+ * Asynchronous on `stream`; returns launch-time errors only. */
+CLCGEMM_API int gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                                 const void *A, const void *B, float *C,
+                                 gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
+                                 int num_workers, void *stream);
 
 /* ---------------------------------------------------------------- misc */
 

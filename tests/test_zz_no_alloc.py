@@ -1,0 +1,62 @@
+"""gemm_run_noalloc: the GEMM for callers that cannot allocate device memory (a process
+whose device memory belongs to its own pool allocator or sits under a hard cap, or a
+latency-critical path that cannot afford a cudaMalloc).  Its scratch is a fixed device
+array inside the library, shared by every call.
+
+Checked through the C ABI against gemm_run (the handle-based entry point) on two calls
+in a row, so the second call also shows that the scratch left behind by the first does
+not leak into its result.  Self-contained: it passes alone in a fresh process and after
+the other tests.  Collected last (file name) so a failure here cannot hide others.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def _reference(g, A, B, tile, cluster, sched):
+    C = torch.full((A.shape[0], B.shape[1]), float("nan"), dtype=torch.float32, device="cuda")
+    g.run(A, B, C, tile=tile, cluster=cluster, sched=sched)
+    g.sync()
+    return C.cpu().numpy()
+
+
+def test_noalloc_matches_gemm_run_on_two_calls():
+    import blackwell_clc_dynamic_gb300 as m
+
+    cases = [
+        # (M, N, K, tile, cluster, sched, seed): the first call covers more tiles than the
+        # second, so stale scratch from call 1 would show up in call 2
+        (1000, 776, 1000, (128, 256, 64), 1, "clc", 91),
+        (384, 512, 256, (128, 128, 64), 1, "static", 92),
+    ]
+    with m.Gemm(0) as g:
+        for M, N, K, tile, cl, sched, seed in cases:
+            A = wl.make_matrix((M, K), seed).cuda()
+            B = wl.make_matrix((K, N), seed + 100).cuda()
+            ref = _reference(g, A, B, tile, cl, sched)
+            C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+            rc = m.gemm_run_noalloc(M, N, K, A, B, C, tile=tile, cluster=cl, sched=sched)
+            assert rc == m.GEMM_OK, m.gemm_strerror(rc)
+            torch.cuda.synchronize()
+            out = C.cpu().numpy()
+            ok, worst = within_tolerance(out, ref.astype(np.float64))
+            assert ok, f"gemm_run_noalloc differs from gemm_run: worst ratio {worst:.3g}"
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    import blackwell_clc_dynamic_gb300 as m
+
+    A = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((128, 256), dtype=torch.float32, device="cuda")
+    # 65537 row tiles x 1 column tile: one tile more than the scratch holds; rejected
+    # before anything is launched, so the small buffers are never touched
+    rc = m.gemm_run_noalloc(128 * 65537, 256, 64, A, B, C)
+    assert rc == m.GEMM_ERR_SCRATCH_LIMIT
+    assert "scratch" in m.gemm_strerror(rc)
+    torch.cuda.synchronize()
