@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--all-out", default=None, help="where --all writes its JSON (default gpurun_out/bench_all.json)")
+    ap.add_argument("--all-steps", type=int, default=60)
     ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent",
                     help="comma-separated subset of the schedules to time (clc is always first)")
     return ap.parse_args()
@@ -346,10 +348,129 @@ def run_ours(args, ws, rank, local):
         "gpu_launches": launches, "clocks": clocks,
     }
     emit(line, args)
+    if args.all:
+        del dA, dB, C
+        torch.cuda.empty_cache()
+        run_extras(g, args, peaks, sms)
     g.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+# ------------------------------------------------------------------ --all: the other workloads
+def time_stream(fn, steps, warmup, stream):
+    """Per-step CUDA-event times on `stream`, synchronising only that stream (an SM
+    occupier may be running on another one)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def summarise(per_ms, flops, min_bytes, peaks):
+    med = statistics.median(per_ms)
+    mean = statistics.mean(per_ms)
+    tf = flops / (mean * 1e-3) / 1e12
+    return {"tflops": tf, "ms_mean": mean, "ms_median": med, "ms_min": min(per_ms), "ms_max": max(per_ms),
+            "pct_bf16_peak_burst": 100 * tf / peaks["bf16_tflops"],
+            "pct_hbm_roofline": 100 * (min_bytes / (mean * 1e-3) / 1e9) / peaks["hbm_gbs"]}
+
+
+def run_extras(g, args, peaks, sms):
+    import torch
+
+    import workloads as wl
+    from oracle import coverage as cv
+
+    out = {"peaks": peaks, "sms": sms, "steps": args.all_steps, "tail": [], "pair": {}, "grouped": {}}
+    steps, warm = args.all_steps, 5
+    st = torch.cuda.Stream()
+
+    # tail sweep: M = 128 T, N = 256, K = 8192 (seed 2): CLC vs static
+    resident = g.max_active_clusters((128, 256, 64), 1)
+    for T in wl.TAIL_T:
+        w = wl.tail(T)
+        A, B = wl.make_inputs(w)
+        dA, dB = A.cuda(), B.cuda()
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        row = {"workload": w.name, "T": T, "tiles": T, "resident": resident,
+               "model_waves": {"clc": math.ceil(T / resident), "static_148": math.ceil(T / 148)}}
+        for key, mode, nw in (("clc", "clc", 0), ("static_148", "static", 148), ("static_sms", "static", sms)):
+            per = time_stream(lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st), steps, warm, st)
+            row[key] = summarise(per, w.flops, w.min_bytes, peaks)
+        out["tail"].append(row)
+        del dA, dB, C
+        torch.cuda.empty_cache()
+
+    # CTA pairs while 24 SMs are held by an occupier on another stream
+    w = wl.PAIR
+    A, B = wl.make_inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    del A, B
+    torch.cuda.synchronize()
+    tiles = (w.M // 256) * (w.N // 256)
+    res_pairs = g.max_active_clusters((128, 256, 64), 2)
+    pair = {"workload": w.name, "cluster_tiles": tiles, "resident_pairs_unoccupied": res_pairs}
+    modes = (("clc", "clc", 0), ("static_74", "static", 74), ("static_sms", "static", sms // 2),
+             ("nonpersistent", "nonpersistent", 0))
+    for occupied in (False, True):
+        so = torch.cuda.Stream()
+        res = {}
+        if occupied:
+            g.occupy_start(24, limit_ns=60_000_000_000, stream=so)
+            g.occupy_wait_resident(10_000)
+        try:
+            for key, mode, nw in modes:
+                per = time_stream(lambda: g.run(dA, dB, C, cluster=2, sched=mode, num_workers=nw, stream=st),
+                                  steps, warm, st)
+                res[key] = summarise(per, w.flops, w.min_bytes, peaks)
+        finally:
+            status = g.occupy_stop() if occupied else 0
+        torch.cuda.synchronize()
+        res["occupier_hit_time_limit"] = bool(status)
+        free_pairs = (sms - (24 if occupied else 0)) // 2
+        res["model_tile_times"] = {
+            "clc": cv.simulate(tiles, cv.CLC, resident=free_pairs).makespan,
+            "static_74": cv.simulate(tiles, cv.STATIC, resident=free_pairs, n_workers=74).makespan,
+            "static_sms": cv.simulate(tiles, cv.STATIC, resident=free_pairs, n_workers=sms // 2).makespan,
+        }
+        pair["occupied_24_sms" if occupied else "all_sms"] = res
+    out["pair"] = pair
+    del dA, dB, C
+    torch.cuda.empty_cache()
+
+    # grouped: 64 problems in one flat grid
+    w = wl.grouped()
+    As, Bs = wl.make_inputs(w)
+    dA = [a.cuda() for a in As]
+    dB = [b.cuda() for b in Bs]
+    del As, Bs
+    dC = [torch.empty((m, w.N), dtype=torch.float32, device="cuda") for m in w.group_m]
+    torch.cuda.synchronize()
+    grp = {"workload": w.name, "problems": len(w.group_m), "rows": sum(w.group_m),
+           "tiles": sum(m // 128 for m in w.group_m) * (w.N // 256)}
+    for key, mode, nw in (("clc", "clc", 0), ("static_148", "static", 148), ("static_sms", "static", sms),
+                          ("nonpersistent", "nonpersistent", 0)):
+        per = time_stream(lambda: g.run_grouped(dA, dB, dC, sched=mode, num_workers=nw, stream=st), steps, warm, st)
+        grp[key] = summarise(per, w.flops, w.min_bytes, peaks)
+    out["grouped"] = grp
+    g.sync(st)
+
+    path = args.all_out or (os.path.join(ROOT, "gpurun_out", "bench_all.json")
+                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "bench_all.json")
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(f"# --all results written to {path}", file=sys.stderr)
 
 
 def main():

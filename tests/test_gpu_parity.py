@@ -203,3 +203,82 @@ def test_run_host_matches_device_run(g):
     g.run_host(A.pin_memory(), B.pin_memory(), Ch)
     g.sync()
     assert_close(Ch.numpy(), oracle.gemm(A, B))
+
+
+_INPUTS = {}
+
+
+def _inputs(w):
+    """Seeded inputs of a full-size workload, drawn once per test session."""
+    if w.name not in _INPUTS:
+        _INPUTS.clear()
+        _INPUTS[w.name] = wl.make_inputs(w)
+    return _INPUTS[w.name]
+
+
+def _sampled_check(A, B, C_dev, M, N, rng, n_entries=512, blocks=()):
+    Ch = C_dev.cpu().numpy()
+    assert not np.isnan(Ch).any(), "an output element was never written"
+    rows = rng.integers(0, M, n_entries)
+    cols = rng.integers(0, N, n_entries)
+    assert_close(Ch[rows, cols], oracle.gemm_entries(A, B, rows, cols))
+    for r0, r1, c0, c1 in blocks:
+        assert_close(Ch[r0:r1, c0:c1], oracle.gemm_block(A, B, r0, r1, c0, c1))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_square_full_size_sampled(g, mode):
+    """M = N = K = 8192 (seed 1), 128 x 256 tiles, the bench's launch configuration."""
+    w = wl.SQUARE
+    A, B = _inputs(w)
+    C = torch.full((w.M, w.N), float("nan"), device="cuda")
+    g.run(A.cuda(), B.cuda(), C, sched=mode, num_workers=148)
+    g.sync()
+    _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(2),
+                   blocks=[(0, 128, 0, 256), (w.M - 128, w.M, w.N - 256, w.N), (4096, 4224, 2048, 2304)])
+    check_log(g, mode, [64], 32, 1, num_workers=148 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_pair_full_size_with_occupied_sms(g, mode):
+    """M = N = 16384, K = 4096, normal(0, 0.02) (seed 3), 256 x 256 cluster tiles on CTA
+    pairs, while an occupier kernel on another stream holds 24 SMs for the whole run."""
+    w = wl.PAIR
+    A, B = _inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.full((w.M, w.N), float("nan"), device="cuda")
+    s_gemm = torch.cuda.Stream()
+    s_occ = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g.occupy_start(24, limit_ns=20_000_000_000, stream=s_occ)
+    try:
+        g.occupy_wait_resident(10_000)
+        g.run(dA, dB, C, cluster=2, sched=mode, num_workers=74, stream=s_gemm)
+        s_gemm.synchronize()
+    finally:
+        timed_out = g.occupy_stop()
+    torch.cuda.synchronize()
+    assert timed_out == 0
+    g.sync()
+    _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(3),
+                   blocks=[(0, 256, 0, 256), (w.M - 256, w.M, w.N - 256, w.N)])
+    check_log(g, mode, [64], 64, 2, num_workers=74 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_grouped_full_size_sampled(g, mode):
+    """64 problems, N = K = 4096, M_g = 128 ceil(lognormal(2, 1)) clipped to [128, 8192]
+    (seed 4), one flat grid of 12096 tiles of 128 x 256: first and last tile of every
+    problem plus scattered elements."""
+    w = wl.grouped()
+    As, Bs = _inputs(w)
+    dA = [a.cuda() for a in As]
+    dB = [b.cuda() for b in Bs]
+    dC = [torch.full((m, w.N), float("nan"), device="cuda") for m in w.group_m]
+    g.run_grouped(dA, dB, dC, sched=mode, num_workers=148)
+    g.sync()
+    rng = np.random.default_rng(4)
+    for a, b, c, m in zip(As, Bs, dC, w.group_m):
+        _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
+                       blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
+    check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
