@@ -22,7 +22,9 @@
  *     of time) are reported by gemm_sync().
  *   - A handle is bound to one device and is not thread-safe.  It owns its workspace
  *     (ownership log, error word, trace buffer, grouped-problem tables, staging buffers
- *     for gemm_run_host) and frees it in gemm_destroy().
+ *     for gemm_run_host) and frees it in gemm_destroy().  A run that needs more
+ *     workspace than earlier runs grows it, and growing synchronises the device first
+ *     (it waits for every stream, including kernels of other libraries).
  *   - Shape rules: M, N, K >= 0; K and N multiples of 8 and all pointers 16-byte aligned
  *     (TMA needs 16-byte row strides and base addresses).  M, N and K need NOT be
  *     multiples of the tile: partial tiles are zero-filled on load and clipped on store.

@@ -249,6 +249,11 @@ def test_pair_full_size_with_occupied_sms(g, mode):
     C = torch.full((w.M, w.N), float("nan"), device="cuda")
     s_gemm = torch.cuda.Stream()
     s_occ = torch.cuda.Stream()
+    # one unoccupied run first: it sizes the handle's log (growing the workspace
+    # synchronises the device, which would wait for the occupier)
+    g.run(dA, dB, C, cluster=2, sched=mode, num_workers=74)
+    g.sync()
+    C.fill_(float("nan"))
     torch.cuda.synchronize()
     g.occupy_start(24, limit_ns=20_000_000_000, stream=s_occ)
     try:
