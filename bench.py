@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--all-out", default=None, help="where --all writes its JSON (default gpurun_out/bench_all.json)")
     ap.add_argument("--all-steps", type=int, default=60)
+    ap.add_argument("--workload", default="square", help="square | pair | grouped | tail<T> | tiny")
+    ap.add_argument("--raster-group", type=int, default=8)
+    ap.add_argument("--l2-prefetch", type=int, default=-1, help="k-blocks prefetched into L2 (-1: library default)")
+    ap.add_argument("--occupy", type=int, default=0, help="SMs held by an occupier kernel while timing")
     ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent",
                     help="comma-separated subset of the schedules to time (clc is always first)")
     return ap.parse_args()
@@ -81,9 +85,9 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_key: str):
+def traffic_for(kernel_key: str, raster_group: int, l2_prefetch: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source."""
+    current kernel source with the same options."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
@@ -92,7 +96,9 @@ def traffic_for(kernel_key: str):
     if d.get("kernel_hash") != kernel_hash():
         return None
     e = d.get("kernels", {}).get(kernel_key)
-    return None if e is None else float(e["dram_bytes_per_launch"])
+    if e is None or e.get("raster_group", 8) != raster_group or e.get("l2_prefetch", 0) != l2_prefetch:
+        return None
+    return float(e["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -205,13 +211,13 @@ def emit(line, args):
 
 
 # ------------------------------------------------------------------ our arm
-def time_steps(fn, steps, warmup, stream, barrier):
+def time_steps(fn, steps, warmup, stream, barrier, sync):
     import torch
     for _ in range(warmup):
         fn()
-    torch.cuda.synchronize()
+    sync()
     barrier()
-    torch.cuda.synchronize()
+    sync()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -221,7 +227,7 @@ def time_steps(fn, steps, warmup, stream, barrier):
         fn()
         ev[i][1].record(stream)
     t1.record(stream)
-    torch.cuda.synchronize()
+    sync()
     barrier()
     per = [a.elapsed_time(b) for a, b in ev]
     return t0.elapsed_time(t1), per
@@ -236,6 +242,22 @@ def cpu_baseline(A, B, seconds):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"rows 0..{rows} of C ({rows}x{B.shape[1]}x{A.shape[1]}), fp64 accumulation, "
                       f"{dt:.1f} s wall"}
+
+
+def make_case(name):
+    """(workload, cluster) for a --workload name."""
+    import workloads as wl
+    if name == "square":
+        return wl.SQUARE, 1
+    if name == "pair":
+        return wl.PAIR, 2
+    if name == "grouped":
+        return wl.grouped(), 1
+    if name.startswith("tail"):
+        return wl.tail(int(name[4:])), 1
+    if name == "tiny":
+        return wl.TINY, 1
+    raise SystemExit(f"unknown workload {name}")
 
 
 def run_ours(args, ws, rank, local):
@@ -254,63 +276,94 @@ def run_ours(args, ws, rank, local):
             dist.barrier()
 
     peaks, peaks_src = load_peaks()
-    w = wl.SQUARE
-    A, B = wl.make_inputs(w, pin=True)
-    dA = A.cuda(non_blocking=True)
-    dB = B.cuda(non_blocking=True)
-    C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-    g = clc.Gemm(local)
-    sms = g.sm_count
+    w, cl = make_case(args.workload)
+    grouped = bool(w.group_m)
     tile = (w.bm, w.bn, 64)
-    resident = g.max_active_clusters(tile, 1)
+    if grouped:
+        As, Bs = wl.make_inputs(w, pin=True)
+        dA = [a.cuda(non_blocking=True) for a in As]
+        dB = [b.cuda(non_blocking=True) for b in Bs]
+        dC = [torch.empty((m, w.N), dtype=torch.float32, device="cuda") for m in w.group_m]
+        A, B = As[0], Bs[0]
+    else:
+        A, B = wl.make_inputs(w, pin=True)
+        dA = A.cuda(non_blocking=True)
+        dB = B.cuda(non_blocking=True)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    # with an occupier running, only stream-level synchronisation may be used
+    stream = torch.cuda.Stream() if args.occupy else torch.cuda.current_stream()
+    g = clc.Gemm(local, raster_group=args.raster_group, l2_prefetch=args.l2_prefetch)
+    sms = g.sm_count
+    resident = g.max_active_clusters(tile, cl)
+    planned = 148 // cl
 
     def step(mode, nw=0):
-        return lambda: g.run(dA, dB, C, tile=tile, cluster=1, sched=mode, num_workers=nw, stream=stream)
+        if grouped:
+            return lambda: g.run_grouped(dA, dB, dC, tile=tile, cluster=cl, sched=mode, num_workers=nw,
+                                         stream=stream)
+        return lambda: g.run(dA, dB, C, tile=tile, cluster=cl, sched=mode, num_workers=nw, stream=stream)
+
+    def sync_all():
+        if args.occupy:
+            stream.synchronize()
+        else:
+            torch.cuda.synchronize()
+
+    wanted = set(args.modes.split(",")) | {"clc"}
+    # "static_148" selects the planned static worker count of the workload's statement
+    # (148 workers, or 74 pairs)
+    order = [(k, m, n) for k, m, n, sel in [("clc", "clc", 0, "clc"),
+                                             (f"static_{planned}", "static", planned, "static_148"),
+                                             ("static_sms", "static", sms // cl, "static_sms"),
+                                             ("nonpersistent", "nonpersistent", 0, "nonpersistent")]
+             if sel in wanted]
+    step("clc")()                     # sizes the handle's workspace before any occupier runs
+    torch.cuda.synchronize()
+    if args.occupy:
+        s_occ = torch.cuda.Stream()
+        g.occupy_start(args.occupy, limit_ns=120_000_000_000, stream=s_occ)
+        g.occupy_wait_resident(10_000)
 
     modes = {}
     clocks = None
     launches = 0
-    wanted = set(args.modes.split(",")) | {"clc"}
-    order = [(k, m, n) for k, m, n in [("clc", "clc", 0), ("static_148", "static", 148),
-                                        ("static_sms", "static", sms), ("nonpersistent", "nonpersistent", 0)]
-             if k in wanted]
-    for key, mode, nw in order:
-        sampler = ClockSampler(local) if key == "clc" else None
-        if sampler:
-            sampler.start()
-        total_ms, per = time_steps(step(mode, nw), args.steps, args.warmup, stream, barrier)
-        if sampler:
-            clocks = sampler.stop()
-        g.sync(stream)
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        if ws > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        tflops = ws * args.steps * w.flops / (total_ms * 1e-3) / 1e12
-        modes[key] = {"tflops": tflops, "ms_per_step": total_ms / args.steps,
-                      "ms_min": min(per), "ms_median": statistics.median(per), "ms_max": max(per),
-                      "pct_bf16_peak_burst": 100.0 * tflops / ws / peaks["bf16_tflops"],
-                      "pct_bf16_peak_sustained": 100.0 * tflops / ws / peaks["bf16_tflops_sustained"],
-                      "workers": nw if mode == "static" else None}
-        if key == "clc":
-            launches = args.steps
-            kernel_ms = statistics.mean(per)
+    kernel_ms = None
+    try:
+        for key, mode, nw in order:
+            sampler = ClockSampler(local) if key == "clc" else None
+            if sampler:
+                sampler.start()
+            total_ms, per = time_steps(step(mode, nw), args.steps, args.warmup, stream, barrier, sync_all)
+            if sampler:
+                clocks = sampler.stop()
+            total_ms = max_over_ranks(total_ms, ws)
+            tflops = ws * args.steps * w.flops / (total_ms * 1e-3) / 1e12
+            modes[key] = {"tflops": tflops, "ms_per_step": total_ms / args.steps,
+                          "ms_min": min(per), "ms_median": statistics.median(per), "ms_max": max(per),
+                          "pct_bf16_peak_burst": 100.0 * tflops / ws / peaks["bf16_tflops"],
+                          "pct_bf16_peak_sustained": 100.0 * tflops / ws / peaks["bf16_tflops_sustained"],
+                          "pct_hbm_roofline": 100.0 * w.min_bytes / (total_ms / args.steps * 1e-3) / 1e9
+                          / peaks["hbm_gbs"],
+                          "workers": nw if mode == "static" else None}
+            if key == "clc":
+                launches = args.steps
+                kernel_ms = statistics.mean(per)
+    finally:
+        occ_status = g.occupy_stop() if args.occupy else 0
+    torch.cuda.synchronize()
+    g.sync(stream)
 
-    # correctness spot check of the timed output (CLC ran first, static/np later wrote C too)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not grouped:
         Ch = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
         n_e2e = max(3, min(20, args.steps // 50))
 
         def e2e_step():
-            g.run_host(A, B, Ch, tile=tile, cluster=1, sched="clc", stream=stream)
-        tot, per = time_steps(e2e_step, n_e2e, 2, stream, barrier)
+            g.run_host(A, B, Ch, tile=tile, cluster=cl, sched="clc", stream=stream)
+        tot, per = time_steps(e2e_step, n_e2e, 2, stream, barrier, torch.cuda.synchronize)
         g.sync(stream)
-        t = torch.tensor([tot], dtype=torch.float64, device="cuda")
-        if ws > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = float(t.item())
+        tot = max_over_ranks(tot, ws)
         e2e = {"value": ws * n_e2e * w.flops / (tot * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": A.numel() * 2 + B.numel() * 2, "d2h_bytes_per_step": Ch.numel() * 4,
                "steps": n_e2e, "ms_per_step": tot / n_e2e, "api": "gemm_run_host (pinned host buffers)"}
@@ -327,35 +380,56 @@ def run_ours(args, ws, rank, local):
 
     clc_m = modes["clc"]
     achieved = w.flops / (kernel_ms * 1e-3) / 1e12
-    traffic = traffic_for("gemm_n256_c1_clc_square")
+    kname = f"gemm_kernel<{w.bn},{cl},CLC>"
+    traffic = traffic_for(f"gemm_n{w.bn}_c{cl}_clc_{args.workload}", args.raster_group, int(g.opts.l2_prefetch))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
             "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": traffic,
             "peak_kind": f"bf16_tflops_sustained ({peaks_src}); timed region is a back-to-back loop",
             "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
             "algorithmic_flops_per_launch": w.flops, "algorithmic_min_bytes_per_launch": w.min_bytes,
-            "kernel": "gemm_kernel<256,1,CLC>"}
+            "kernel": kname}
+    big = w.min_bytes > 129e6
     line = {
         "metric": METRIC, "value": clc_m["tflops"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": clc_m["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32",
-        "data": "synthetic (seeded uniform[-1,1] bf16)",
+        "data": "synthetic (seeded bf16, see workloads.py)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "tile": list(tile),
-                   "cluster": [1, 1, 1], "sched": "clc", "parallelism": f"replicas x{ws}",
-                   "l2": "no flush: inputs (A+B 256 MiB) and C (256 MiB) exceed the 129 MB L2",
+                   "cluster": [cl, 1, 1], "sched": "clc", "parallelism": f"replicas x{ws}",
+                   "raster_group": args.raster_group, "l2_prefetch": int(g.opts.l2_prefetch),
+                   "occupied_sms": args.occupy,
+                   "l2": ("no flush: operands and C exceed the 129 MB L2" if big
+                          else "no flush (small case; parity only)"),
                    "sms": sms, "resident_clusters": resident},
-        "pct_of_bf16_peak": 100.0 * clc_m["tflops"] / ws / peaks["bf16_tflops_sustained"],
+        "pct_of_bf16_peak_burst": clc_m["pct_bf16_peak_burst"],
+        "pct_of_bf16_peak_sustained": clc_m["pct_bf16_peak_sustained"],
         "modes": modes, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "clocks": clocks,
     }
+    if args.occupy:
+        line["occupier_hit_time_limit"] = bool(occ_status)
     emit(line, args)
     if args.all:
-        del dA, dB, C
+        if grouped:
+            del dA, dB, dC
+        else:
+            del dA, dB, C
         torch.cuda.empty_cache()
         run_extras(g, args, peaks, sms)
     g.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def max_over_ranks(x, ws):
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ------------------------------------------------------------------ --all: the other workloads

@@ -60,6 +60,7 @@ struct Params {
   int* err;                      // device error word
   long long timeout_ns;          // bound on every wait
   int inject_fail_after;         // CLC: stop after this many successful cancels (<0: off)
+  int l2_prefetch;               // k-blocks the producer prefetches into L2 ahead of its loads (0: off)
 };
 
 template <int BN_, int CL_>
@@ -323,8 +324,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
         const int ay = w.m_blk * BM;
         const int bx = w.n_blk * BN + (int)rank * C::BN_CTA;
+        const int pf = p.l2_prefetch;
+        auto prefetch = [&](int kq) {
+          tma_prefetch_l2_2d(mA, kq * BK, ay);
+#pragma unroll
+          for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_l2_2d(mB, bx + 64 * j, kq * BK);
+        };
+        for (int kq = C::STAGES; kq < pf && kq < p.k_blocks; ++kq) prefetch(kq);
         bool ok = true;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (pf > 0 && kb + pf < p.k_blocks && kb + pf >= C::STAGES) prefetch(kb + pf);
           if (!bar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, p, ctl, WAIT_EMPTY)) { ok = false; break; }
           if (rank == 0) mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TX_BYTES);
           const uint32_t a_dst = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;

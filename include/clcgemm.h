@@ -88,6 +88,8 @@ typedef struct {
                                   scheduler reports a failed fetch without issuing a cancel;
                                   < 0 (default) disables it */
     int     raster_group;      /* tile rows per raster band; <= 0 selects 8; 1 = row-major */
+    int     l2_prefetch;       /* k-blocks (of 64) the producer prefetches into L2 ahead of its
+                                  loads; 0 = off, < 0 selects the default */
 } gemm_opts_t;
 
 /* Description of the last launch, filled by gemm_last_launch(). */
