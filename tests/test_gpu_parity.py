@@ -287,3 +287,18 @@ def test_grouped_full_size_sampled(g, mode):
         _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
                        blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
     check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+def test_run_host_banded_pipeline(g, tile, cl):
+    """gemm_run_host splits A into row bands (a ragged last band here) and overlaps the
+    copies with the band GEMMs on several streams; the result must equal the oracle."""
+    M, N, K = 5000, 776, 512
+    A = wl.make_matrix((M, K), 83).pin_memory()
+    B = wl.make_matrix((K, N), 84).pin_memory()
+    Ch = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream()
+    g.run_host(A, B, Ch, tile=tile, cluster=cl, stream=s)
+    s.synchronize()
+    g.sync(s)
+    assert_close(Ch.numpy(), oracle.gemm(A, B))
