@@ -458,6 +458,42 @@ def summarise(per_ms, flops, min_bytes, peaks):
             "pct_hbm_roofline": 100 * (min_bytes / (mean * 1e-3) / 1e9) / peaks["hbm_gbs"]}
 
 
+def trace_stats(g, run_once):
+    """One traced run: per-tile CLC waits and round trips, per-SM active span.  Only the
+    run's own stream is synchronised (an occupier may hold other SMs meanwhile); the
+    trace buffer must already be large enough (a traced run of the same size happened
+    before any occupier started), since growing it synchronises the device."""
+    g.set_opts(trace_enable=1)
+    try:
+        run_once()
+        tr = g.get_trace().astype(np.int64)
+    finally:
+        g.set_opts(trace_enable=0)
+    start, end, sm = tr[:, 0], tr[:, 1], tr[:, 2]
+    ok = (start > 0) & (end > 0)
+    t0 = start[ok].min()
+    span = {}
+    for s_, e_, m_ in zip(start[ok], end[ok], sm[ok]):
+        a, b = span.get(int(m_), (s_, e_))
+        span[int(m_)] = (min(a, s_), max(b, e_))
+    busy = np.array([b - a for a, b in span.values()], dtype=np.float64)
+    last = np.array([b - t0 for a, b in span.values()], dtype=np.float64)
+    wait = tr[:, 4][tr[:, 4] > 0].astype(np.float64)
+    rt = tr[:, 5][tr[:, 5] > 0].astype(np.float64)
+
+    def q(x):
+        if x.size == 0:
+            return None
+        return {"n": int(x.size), "mean_us": float(x.mean() / 1e3), "p50_us": float(np.percentile(x, 50) / 1e3),
+                "p99_us": float(np.percentile(x, 99) / 1e3), "max_us": float(x.max() / 1e3)}
+    return {"sms_used": len(span), "kernel_span_us": float((end[ok].max() - t0) / 1e3),
+            "sm_active_span_us": {"min": float(busy.min() / 1e3), "mean": float(busy.mean() / 1e3),
+                                  "max": float(busy.max() / 1e3)},
+            "sm_last_end_us": {"min": float(last.min() / 1e3), "max": float(last.max() / 1e3)},
+            "tile_us": q((end[ok] - start[ok]).astype(np.float64)),
+            "producer_wait_for_clc_response": q(wait), "try_cancel_round_trip": q(rt)}
+
+
 def run_extras(g, args, peaks, sms):
     import torch
 
@@ -481,6 +517,8 @@ def run_extras(g, args, peaks, sms):
         for key, mode, nw in (("clc", "clc", 0), ("static_148", "static", 148), ("static_sms", "static", sms)):
             per = time_stream(lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st), steps, warm, st)
             row[key] = summarise(per, w.flops, w.min_bytes, peaks)
+            if T in (149, 297) and key != "static_sms":
+                row[key]["trace"] = trace_stats(g, lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st))
         out["tail"].append(row)
         del dA, dB, C
         torch.cuda.empty_cache()
@@ -508,6 +546,9 @@ def run_extras(g, args, peaks, sms):
                 per = time_stream(lambda: g.run(dA, dB, C, cluster=2, sched=mode, num_workers=nw, stream=st),
                                   steps, warm, st)
                 res[key] = summarise(per, w.flops, w.min_bytes, peaks)
+                if key in ("clc", "static_74"):
+                    res[key]["trace"] = trace_stats(
+                        g, lambda: g.run(dA, dB, C, cluster=2, sched=mode, num_workers=nw, stream=st))
         finally:
             status = g.occupy_stop() if occupied else 0
         torch.cuda.synchronize()
@@ -537,6 +578,9 @@ def run_extras(g, args, peaks, sms):
                           ("nonpersistent", "nonpersistent", 0)):
         per = time_stream(lambda: g.run_grouped(dA, dB, dC, sched=mode, num_workers=nw, stream=st), steps, warm, st)
         grp[key] = summarise(per, w.flops, w.min_bytes, peaks)
+        if key in ("clc", "static_148"):
+            grp[key]["trace"] = trace_stats(g, lambda: g.run_grouped(dA, dB, dC, sched=mode, num_workers=nw,
+                                                                     stream=st))
     out["grouped"] = grp
     g.sync(st)
 

@@ -53,7 +53,8 @@ class gemm_cluster_t(ctypes.Structure):
 
 class gemm_opts_t(ctypes.Structure):
     _fields_ = [("log_enable", ctypes.c_int), ("trace_enable", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
-                ("inject_fail_after", ctypes.c_int), ("raster_group", ctypes.c_int), ("l2_prefetch", ctypes.c_int)]
+                ("inject_fail_after", ctypes.c_int), ("raster_group", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
+                ("hold_scheduler", ctypes.c_int)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
@@ -219,9 +220,10 @@ class Gemm:
     """One library handle on one device."""
 
     def __init__(self, device: int = 0, log: bool = True, trace: bool = False, timeout_ns: int = 0,
-                 inject_fail_after: int = -1, raster_group: int = 8, l2_prefetch: int = -1):
+                 inject_fail_after: int = -1, raster_group: int = 8, l2_prefetch: int = -1,
+                 hold_scheduler: bool = False):
         self.opts = gemm_opts_t(int(log), int(trace), int(timeout_ns), int(inject_fail_after), int(raster_group),
-                                int(l2_prefetch))
+                                int(l2_prefetch), int(hold_scheduler))
         rc, h = gemm_create(device, self.opts)
         _check(rc, "gemm_create")
         self.h = h
@@ -293,7 +295,7 @@ class Gemm:
     def get_trace(self):
         import numpy as np
         info = self.last_launch()
-        out = np.empty((info["n_tiles"], 4), dtype=np.uint64)
+        out = np.empty((info["n_tiles"], 8), dtype=np.uint64)
         _check(lib.gemm_get_trace(self.h, out.ctypes.data, info["n_tiles"]), "gemm_get_trace")
         return out
 

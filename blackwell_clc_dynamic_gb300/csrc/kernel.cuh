@@ -33,6 +33,7 @@ constexpr int CLC_DEPTH = 3;     // response ring depth
 constexpr int THR_DEPTH = 3;     // throttle ring depth
 constexpr int EPI_WARP0 = 4;
 constexpr int EPI_CHUNK = 32;    // fp32 columns per epilogue store
+constexpr int TRACE_WORDS = 8;   // u64 per CTA tile in the optional trace
 
 // Device error word: [0] bits, [1] first failing wait site, [2] block of that wait.
 enum : int { ERRB_TIMEOUT = 1 };
@@ -56,11 +57,13 @@ struct Params {
   int* log_owner;                // [CTA tiles] worker that computed the tile (or null)
   int* log_claims;               // [CTA tiles] times the tile was computed
   int* log_first;                // [launched workers] linear id of the worker's first tile
-  unsigned long long* trace;     // [CTA tiles][4] start ns, end ns, smid, worker (or null)
+  unsigned long long* trace;     // [CTA tiles][8]: start ns, end ns, smid, worker, producer's wait
+                                 // for this tile's CLC response (ns), try_cancel round trip (ns)
   int* err;                      // device error word
   long long timeout_ns;          // bound on every wait
   int inject_fail_after;         // CLC: stop after this many successful cancels (<0: off)
   int l2_prefetch;               // k-blocks the producer prefetches into L2 ahead of its loads (0: off)
+  int hold_scheduler;            // test hook: the CLC scheduler issues and signals nothing
 };
 
 template <int BN_, int CL_>
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if (!bar_wait(bar(C::BAR_THR_EMPTY + t), ((tile / THR_DEPTH) & 1) ^ 1, p, ctl, WAIT_THR_EMPTY)) break;
           mbar_arrive(bar(C::BAR_THR_FULL + t));
         }
-        if (p.trace) p.trace[4 * (size_t)w.pos + 0] = globaltimer();
+        if (p.trace) p.trace[TRACE_WORDS * (size_t)w.pos + 0] = globaltimer();
         const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;
         const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
         const int ay = w.m_blk * BM;
@@ -354,7 +357,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
         if (!ok) break;
         ++tile;
+        const uint64_t t_req = p.trace ? globaltimer() : 0;
         w = it.next(p, rank, sb, ctl, false);
+        if (p.trace && w.valid) p.trace[TRACE_WORDS * (size_t)w.pos + 4] = globaltimer() - t_req;
       }
     }
     __syncwarp();
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ CLC scheduler
-    if (SCHED == SCHED_CLC && rank == 0 && elect_one()) {
+    if (SCHED == SCHED_CLC && rank == 0 && !p.hold_scheduler && elect_one()) {
       int s = 0;
       uint32_t ph = 0;
       for (int r = 0;; ++r) {
@@ -410,6 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const uint32_t full = bar(C::BAR_CLC_FULL + s);
         const uint32_t resp = sb + C::OFF_RESP + 16u * (uint32_t)s;
         const bool inject = p.inject_fail_after >= 0 && r >= p.inject_fail_after;
+        const uint64_t t_issue = p.trace ? globaltimer() : 0;
         if (!inject) {
           mbar_arrive_expect_tx(full, 16);
           if constexpr (CL == 1) {
@@ -431,9 +437,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         // the scheduler consumes the response too: it stops at the first failure
         bool ok = false;
         if (bar_wait(full, ph, p, ctl, WAIT_CLC_FULL)) {
-          uint32_t x;
+          uint32_t x = 0;
           if (misc[2 + s] == 0) ok = clc_decode(resp, x);
           fence_proxy_async_smem();
+          if (ok && p.trace) {
+            const Work got = make_work<CL>(p, (int)(x / CL), 0);
+            if (got.valid) p.trace[TRACE_WORDS * (size_t)got.pos + 5] = globaltimer() - t_issue;
+          }
         }
         mbar_arrive(bar(C::BAR_CLC_EMPTY + s));
         if (++s == CLC_DEPTH) { s = 0; ph ^= 1; }
@@ -502,9 +512,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if (first_tile && rank == 0) p.log_first[worker] = w.c;
         }
         if (p.trace) {
-          p.trace[4 * (size_t)w.pos + 1] = globaltimer();
-          p.trace[4 * (size_t)w.pos + 2] = smid();
-          p.trace[4 * (size_t)w.pos + 3] = (unsigned long long)worker;
+          p.trace[TRACE_WORDS * (size_t)w.pos + 1] = globaltimer();
+          p.trace[TRACE_WORDS * (size_t)w.pos + 2] = smid();
+          p.trace[TRACE_WORDS * (size_t)w.pos + 3] = (unsigned long long)worker;
         }
       }
       first_tile = false;

@@ -89,7 +89,11 @@ typedef struct {
                                   < 0 (default) disables it */
     int     raster_group;      /* tile rows per raster band; <= 0 selects 8; 1 = row-major */
     int     l2_prefetch;       /* k-blocks (of 64) the producer prefetches into L2 ahead of its
-                                  loads; 0 = off, < 0 selects the default */
+                                  loads; 0 = off (default), < 0 selects the default */
+    int     hold_scheduler;    /* test hook (default 0): in CLC mode the scheduler issues no
+                                  cancel and signals nothing, so every response wait runs out
+                                  after timeout_ns; each worker computes its own tile and
+                                  gemm_sync reports GEMM_ERR_TIMEOUT */
 } gemm_opts_t;
 
 /* Description of the last launch, filled by gemm_last_launch(). */
@@ -171,7 +175,8 @@ CLCGEMM_API int gemm_device_error(gemm_handle_t h, int32_t out3[3]);
 /* gemm_last_launch: shape of the most recent launch (its log sizes). */
 CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
 
-/* gemm_get_log: synchronous copy-out of the most recent run's ownership log.
+/* gemm_get_log: copy-out of the most recent run's ownership log; waits for that run's
+ * stream only (pageable `owner`/`claims`/`first` memory is fine).
  *   owner[n_tiles]     worker (cluster launch id) that computed each CTA tile
  *   claims[n_tiles]    how many times each CTA tile was computed (1 when correct)
  *   first[n_workers]   linear id of each worker's first tile, -1 if the worker never ran
@@ -181,9 +186,13 @@ CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
 CLCGEMM_API int gemm_get_log(gemm_handle_t h, int32_t *owner, int32_t *claims, int32_t *first,
                  int64_t n_tiles, int64_t n_workers);
 
-/* gemm_get_trace: synchronous copy-out of the trace of the most recent run (requires
- * trace_enable): 4 x uint64 per CTA tile: start ns, end ns (device globaltimer), SM id,
- * worker. */
+/* gemm_get_trace: copy-out of the trace of the most recent run, waiting for its stream (requires
+ * trace_enable): 8 x uint64 per CTA tile (out holds n_tiles * 8):
+ *   [0] start ns (the producer begins the tile; device globaltimer)  [1] end ns (the
+ *   epilogue issued the tile's last store)  [2] SM id  [3] worker  [4] ns the producer
+ *   waited for the CLC response that named this tile (0 for a worker's first tile and
+ *   for the other schedules)  [5] ns from the try_cancel that returned this tile to the
+ *   scheduler seeing its response (CLC, rank-0 tile only)  [6], [7] zero. */
 CLCGEMM_API int gemm_get_trace(gemm_handle_t h, uint64_t *out, int64_t n_tiles);
 
 /* ---------------------------------------------------------------- occupancy */

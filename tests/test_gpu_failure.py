@@ -1,0 +1,46 @@
+"""Failure detection without a GPU fault: every device-side wait is bounded, and a wait
+that runs out is reported through the device error word while the context stays usable.
+
+The hold_scheduler hook makes the CLC scheduler issue and signal nothing (a response
+that nothing ever delivers).  Every worker still computes its own launch's tile, then
+its response waits run out after timeout_ns; nothing is in flight by then (the tile
+finished microseconds earlier), so the CTA unwinds, frees its tensor memory and exits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests.gpu_helpers import TILE_256, assert_close, check_log
+
+pytestmark = pytest.mark.gpu
+
+WAIT_CLC_FULL = 5
+
+
+@pytest.mark.parametrize("cl", [1, 2], ids=["c1", "c2"])
+def test_response_wait_times_out_and_is_reported(cl):
+    import blackwell_clc_dynamic_gb300 as m
+    M, N, K = 128 * cl * 6, 512, 256
+    A = wl.make_matrix((M, K), 101)
+    B = wl.make_matrix((K, N), 102)
+    with m.Gemm(0, timeout_ns=50_000_000, hold_scheduler=True) as g:
+        C = torch.full((M, N), float("nan"), device="cuda")
+        g.run(A.cuda(), B.cuda(), C, tile=TILE_256, cluster=cl, sched="clc")
+        torch.cuda.synchronize()
+        bits, site, block = g.device_error()
+        assert bits == 1 and site == WAIT_CLC_FULL
+        with pytest.raises(m.GemmError) as ei:
+            g.sync()
+        assert ei.value.code == m.GEMM_ERR_TIMEOUT
+        # nothing was stolen: every launch computed its own tile, exactly once
+        assert_close(C.cpu().numpy(), oracle.gemm(A, B))
+        owner_lin, first = check_log(g, "nonpersistent", [6], 2, cl)
+        # the error word was cleared by gemm_sync, and the context still works
+        g.set_opts(hold_scheduler=0, timeout_ns=0)
+        C2 = torch.full((M, N), float("nan"), device="cuda")
+        g.run(A.cuda(), B.cuda(), C2, tile=TILE_256, cluster=cl, sched="clc")
+        g.sync()
+        assert g.device_error() == (0, 0, 0)
+        assert_close(C2.cpu().numpy(), oracle.gemm(A, B))
