@@ -193,7 +193,10 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed},
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "tile": [w.bm, w.bn, 64],
+                   "cluster": [1, 1, 1], "sched": "clc", "parallelism": f"replicas x{ws}",
+                   "l2": "no flush: operands and C exceed the 129 MB L2",
+                   "arm": "CPU oracle (fp64) on the host cores: the pages ship no code to run"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{rows} rows of C ({rows}x{w.N}x{w.K}) per step, fp64 accumulation"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
