@@ -150,13 +150,15 @@ CLCGEMM_API int gemm_run_grouped(gemm_handle_t h, int G, const int64_t *M_g, int
                      gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
                      int num_workers, void *stream);
 
-/* gemm_run_host: the same product from HOST buffers.  B is copied to a device staging
- * buffer owned by the handle while A is copied in bands of rows; each band's GEMM starts
- * as soon as its rows have arrived, and each band of C is copied back to C_host while
- * later bands compute (handle-owned streams, ordered after earlier work on `stream`;
- * `stream` waits for the last copy).  Pinned host memory makes the copies asynchronous.
- * The first call (or a larger problem) allocates the staging buffers.  The ownership log
- * afterwards describes the last band. */
+/* gemm_run_host: the same product from HOST buffers.  A and B are copied to device
+ * staging buffers owned by the handle in blocks (row bands of A, column bands of B, up
+ * to 8 each, about 2048 wide); the GEMM of each C block starts as soon as its A and B
+ * bands have arrived, and each C block is copied back to C_host while later blocks
+ * compute, so host-to-device and device-to-host copies run at the same time (handle-owned
+ * streams, ordered after earlier work on `stream`; `stream` waits for the last copy).
+ * Pinned host memory makes the copies asynchronous.  The first call (or a larger
+ * problem) allocates the staging buffers.  The ownership log afterwards describes the
+ * last block. */
 CLCGEMM_API int gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                   const void *A_host, const void *B_host, float *C_host,
                   gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,

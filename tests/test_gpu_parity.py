@@ -291,9 +291,10 @@ def test_grouped_full_size_sampled(g, mode):
 
 @pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
 def test_run_host_banded_pipeline(g, tile, cl):
-    """gemm_run_host splits A into row bands (a ragged last band here) and overlaps the
-    copies with the band GEMMs on several streams; the result must equal the oracle."""
-    M, N, K = 5000, 776, 512
+    """gemm_run_host splits the product into blocks (2 row bands x 2 column bands here, the
+    last of each ragged), copies them with strided copies and overlaps the copies with the
+    block GEMMs on several streams; the result must equal the oracle."""
+    M, N, K = 4200, 4104, 256
     A = wl.make_matrix((M, K), 83).pin_memory()
     B = wl.make_matrix((K, N), 84).pin_memory()
     Ch = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
