@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--all-out", default=None, help="where --all writes its JSON (default gpurun_out/bench_all.json)")
     ap.add_argument("--all-steps", type=int, default=60)
-    ap.add_argument("--workload", default="square", help="square | pair | grouped | tail<T> | tiny")
+    ap.add_argument("--workload", default="square", help="square | pair | grouped | grouped_vk | tail<T> | tiny")
     ap.add_argument("--raster-group", type=int, default=8)
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="k-blocks prefetched into L2 (-1: library default)")
     ap.add_argument("--occupy", type=int, default=0, help="SMs held by an occupier kernel while timing")
@@ -256,6 +256,8 @@ def make_case(name):
         return wl.PAIR, 2
     if name == "grouped":
         return wl.grouped(), 1
+    if name == "grouped_vk":
+        return wl.grouped_varied_depth(), 1
     if name.startswith("tail"):
         return wl.tail(int(name[4:])), 1
     if name == "tiny":
@@ -303,8 +305,8 @@ def run_ours(args, ws, rank, local):
 
     def step(mode, nw=0):
         if grouped:
-            return lambda: g.run_grouped(dA, dB, dC, tile=tile, cluster=cl, sched=mode, num_workers=nw,
-                                         stream=stream)
+            return lambda: g.run_grouped_v(dA, dB, dC, tile=tile, cluster=cl, sched=mode, num_workers=nw,
+                                           stream=stream)
         return lambda: g.run(dA, dB, C, tile=tile, cluster=cl, sched=mode, num_workers=nw, stream=stream)
 
     def sync_all():
@@ -585,6 +587,38 @@ def run_extras(g, args, peaks, sms):
             grp[key]["trace"] = trace_stats(g, lambda: g.run_grouped(dA, dB, dC, sched=mode, num_workers=nw,
                                                                      stream=st))
     out["grouped"] = grp
+    g.sync(st)
+    del dA, dB, dC
+    torch.cuda.empty_cache()
+
+    # grouped problems of different depth: tiles of unequal cost
+    w = wl.grouped_varied_depth()
+    As, Bs = wl.make_inputs(w)
+    dA = [a.cuda() for a in As]
+    dB = [b.cuda() for b in Bs]
+    del As, Bs
+    dC = [torch.empty((m, w.N), dtype=torch.float32, device="cuda") for m in w.group_m]
+    torch.cuda.synchronize()
+    cost = []
+    for m, k in zip(w.group_m, w.depths()):
+        cost += [k / 64] * ((m // 128) * (w.N // 256))
+    T = len(cost)
+    vk = {"workload": w.name, "problems": len(w.group_m), "rows": sum(w.group_m), "tiles": T,
+          "k_min": min(w.depths()), "k_max": max(w.depths()),
+          "model_makespan_kblocks": {
+              "clc": cv.simulate(T, cv.CLC, resident=sms, cost=cost).makespan,
+              "static_148": cv.simulate(T, cv.STATIC, resident=sms, n_workers=148, cost=cost).makespan,
+              "static_sms": cv.simulate(T, cv.STATIC, resident=sms, n_workers=sms, cost=cost).makespan,
+              "ideal": sum(cost) / sms}}
+    for key, mode, nw in (("clc", "clc", 0), ("static_148", "static", 148), ("static_sms", "static", sms),
+                          ("nonpersistent", "nonpersistent", 0)):
+        per = time_stream(lambda: g.run_grouped_v(dA, dB, dC, sched=mode, num_workers=nw, stream=st), steps, warm,
+                          st)
+        vk[key] = summarise(per, w.flops, w.min_bytes, peaks)
+        if key in ("clc", "static_148"):
+            vk[key]["trace"] = trace_stats(g, lambda: g.run_grouped_v(dA, dB, dC, sched=mode, num_workers=nw,
+                                                                      stream=st))
+    out["grouped_varied_depth"] = vk
     g.sync(st)
 
     path = args.all_out or (os.path.join(ROOT, "gpurun_out", "bench_all.json")

@@ -39,7 +39,7 @@ EXPORTS = (
     "gemm_opts_default", "gemm_create", "gemm_destroy", "gemm_set_opts", "gemm_run", "gemm_run_grouped",
     "gemm_run_host", "gemm_sync", "gemm_device_error", "gemm_last_launch", "gemm_get_log", "gemm_get_trace",
     "gemm_max_active_clusters", "gemm_sm_count", "gemm_occupy_start", "gemm_occupy_wait_resident",
-    "gemm_occupy_stop", "gemm_strerror", "gemm_version", "gemm_run_noalloc",
+    "gemm_occupy_stop", "gemm_strerror", "gemm_version", "gemm_run_noalloc", "gemm_run_grouped_v",
 )
 
 
@@ -83,6 +83,9 @@ def _load() -> ctypes.CDLL:
         "gemm_run": (i32, [H, i64, i64, i64, p, p, p, gemm_tile_t, gemm_cluster_t, i32, i32, p]),
         "gemm_run_grouped": (i32, [H, i32, ctypes.POINTER(i64), i64, i64, ctypes.POINTER(p), ctypes.POINTER(p),
                                    ctypes.POINTER(p), gemm_tile_t, gemm_cluster_t, i32, i32, p]),
+        "gemm_run_grouped_v": (i32, [H, i32, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                     ctypes.POINTER(p), ctypes.POINTER(p), ctypes.POINTER(p), gemm_tile_t,
+                                     gemm_cluster_t, i32, i32, p]),
         "gemm_run_host": (i32, [H, i64, i64, i64, p, p, p, gemm_tile_t, gemm_cluster_t, i32, i32, p]),
         "gemm_sync": (i32, [H, p]),
         "gemm_device_error": (i32, [H, ctypes.POINTER(ctypes.c_int32)]),
@@ -211,6 +214,19 @@ def gemm_run_noalloc(M, N, K, A, B, C, tile=(128, 256, 64), cluster=1, sched="cl
                                 num_workers, _stream(stream))
 
 
+def gemm_run_grouped_v(h, M_g: Sequence[int], N_g: Sequence[int], K_g: Sequence[int], A_g, B_g, C_g,
+                       tile=(128, 256, 64), cluster=1, sched="clc", num_workers=0, stream=None) -> int:
+    G = len(M_g)
+    m = (ctypes.c_int64 * G)(*M_g)
+    n = (ctypes.c_int64 * G)(*N_g)
+    k = (ctypes.c_int64 * G)(*K_g)
+    a = (ctypes.c_void_p * G)(*[_ptr(x) for x in A_g])
+    b = (ctypes.c_void_p * G)(*[_ptr(x) for x in B_g])
+    c = (ctypes.c_void_p * G)(*[_ptr(x) for x in C_g])
+    return lib.gemm_run_grouped_v(h, G, m, n, k, a, b, c, _tile(tile), _cluster(cluster), _sched(sched),
+                                  num_workers, _stream(stream))
+
+
 def gemm_sync(h, stream=None) -> int:
     return lib.gemm_sync(h, _stream(stream))
 
@@ -268,6 +284,15 @@ class Gemm:
         N = Bs[0].shape[1] if Bs else 0
         _check(gemm_run_grouped(self.h, M_g, N, K, As, Bs, Cs, tile, cluster, sched, num_workers, stream),
                "gemm_run_grouped")
+
+    def run_grouped_v(self, As, Bs, Cs, tile=(128, 256, 64), cluster=1, sched="clc", num_workers=0,
+                      stream=None) -> None:
+        """Problems of different shapes: C_g = A_g @ B_g with A_g (M_g x K_g), B_g (K_g x N_g)."""
+        M_g = [a.shape[0] for a in As]
+        K_g = [a.shape[1] for a in As]
+        N_g = [b.shape[1] for b in Bs]
+        _check(gemm_run_grouped_v(self.h, M_g, N_g, K_g, As, Bs, Cs, tile, cluster, sched, num_workers, stream),
+               "gemm_run_grouped_v")
 
     def sync(self, stream=None) -> None:
         _check(gemm_sync(self.h, stream), "gemm_sync")

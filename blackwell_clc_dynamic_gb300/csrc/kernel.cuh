@@ -49,8 +49,10 @@ struct Params {
   const CUtensorMap* gmaps;      // grouped: (A, B, C) per problem in device memory
   const int* g_tile_start;       // grouped: G+1 prefix sums of cluster tiles
   const int* g_mt;               // grouped: cluster-tile rows of each problem
+  const int* g_nt;               // grouped: tile columns of each problem
+  const int* g_kb;               // grouped: k-blocks (ceil(K_g / 64)) of each problem
   int G;                         // number of problems (0: plain problem in tmA/tmB/tmC)
-  int mt, nt;                    // cluster-tile grid of the plain problem; nt for all
+  int mt, nt;                    // cluster-tile grid of the plain problem
   int total;                     // cluster tiles in the launch
   int k_blocks;                  // ceil(K / 64)
   int raster_group;              // tile rows per raster band
@@ -129,6 +131,7 @@ struct Work {
   int m_blk;   // this CTA's 128-row block inside its problem
   int n_blk;   // BN-column block
   int pos;     // ownership-log index of this CTA's tile
+  int kb;      // k-blocks of this tile's problem
   bool valid;
 };
 
@@ -150,8 +153,9 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
   w.m_blk = 0;
   w.n_blk = 0;
   w.pos = 0;
+  w.kb = 0;
   if (!w.valid) return w;
-  int base = 0, mt = p.mt, g = 0;
+  int base = 0, mt = p.mt, nt = p.nt, kb = p.k_blocks, g = 0;
   if (p.G > 0) {
     int lo = 0, hi = p.G - 1;   // largest g with start[g] <= c
     while (lo < hi) {
@@ -161,13 +165,16 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
     g = lo;
     base = __ldg(p.g_tile_start + g);
     mt = __ldg(p.g_mt + g);
+    nt = __ldg(p.g_nt + g);
+    kb = __ldg(p.g_kb + g);
   }
   int m, n;
-  raster_map(c - base, mt, p.nt, p.raster_group, m, n);
+  raster_map(c - base, mt, nt, p.raster_group, m, n);
   w.g = g;
   w.m_blk = m * CL + (int)rank;
   w.n_blk = n;
-  w.pos = base * CL + w.m_blk * p.nt + n;
+  w.pos = base * CL + w.m_blk * nt + n;
+  w.kb = kb;
   return w;
 }
 
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     for (int i = 1; i < 8; ++i) misc[i] = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0 && p.G == 0) {
+  if (warp == 0 && lane == 0 && p.G == 0 && p.k_blocks > 0) {
     prefetch_tmap(&p.tmA);
     prefetch_tmap(&p.tmB);
     prefetch_tmap(&p.tmC);
@@ -333,10 +340,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_l2_2d(mB, bx + 64 * j, kq * BK);
         };
-        for (int kq = C::STAGES; kq < pf && kq < p.k_blocks; ++kq) prefetch(kq);
+        for (int kq = C::STAGES; kq < pf && kq < w.kb; ++kq) prefetch(kq);
         bool ok = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (pf > 0 && kb + pf < p.k_blocks && kb + pf >= C::STAGES) prefetch(kb + pf);
+        for (int kb = 0; kb < w.kb; ++kb) {
+          if (pf > 0 && kb + pf < w.kb && kb + pf >= C::STAGES) prefetch(kb + pf);
           if (!bar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, p, ctl, WAIT_EMPTY)) { ok = false; break; }
           if (rank == 0) mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TX_BYTES);
           const uint32_t a_dst = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < w.kb; ++kb) {
           if (!bar_wait(bar(C::BAR_FULL + s), ph, p, ctl, WAIT_FULL)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             else mbar_arrive_cluster(acc_empty_leader0 + 8u * (uint32_t)acc);
           }
         }
-        if (p.k_blocks == 0) {
+        if (w.kb == 0) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0u;
         }

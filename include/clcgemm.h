@@ -150,6 +150,16 @@ CLCGEMM_API int gemm_run_grouped(gemm_handle_t h, int G, const int64_t *M_g, int
                      gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
                      int num_workers, void *stream);
 
+/* gemm_run_grouped_v: like gemm_run_grouped, but every problem has its own shape:
+ * C_g (M_g x N_g) = A_g (M_g x K_g) * B_g (K_g x N_g); each N_g and K_g a multiple of 8.
+ * Tiles of different problems then cost different amounts of work (K_g / 64 k-steps),
+ * which is where run-time work stealing pays.  The ownership log indexes each problem's
+ * CTA tiles row-major over (M_g / 128) x (N_g / bn), problems in order. */
+CLCGEMM_API int gemm_run_grouped_v(gemm_handle_t h, int G, const int64_t *M_g, const int64_t *N_g,
+                                   const int64_t *K_g, const void *const *A_g, const void *const *B_g,
+                                   float *const *C_g, gemm_tile_t tile, gemm_cluster_t cluster,
+                                   gemm_sched_t sched, int num_workers, void *stream);
+
 /* gemm_run_host: the same product from HOST buffers.  A and B are copied to device
  * staging buffers owned by the handle in blocks (row bands of A, column bands of B, up
  * to 8 each, about 2048 wide); the GEMM of each C block starts as soon as its A and B

@@ -66,17 +66,19 @@ def raster(c: int, mt: int, nt: int, group_rows: int = 8) -> Tuple[int, int]:
     return band * group_rows + r % rows_in_band, r // rows_in_band
 
 
-def grouped_tile(c: int, tiles_m: Sequence[int], nt: int, group_rows: int = 8) -> Tuple[int, int, int]:
+def grouped_tile(c: int, tiles_m: Sequence[int], nt, group_rows: int = 8) -> Tuple[int, int, int]:
     """Flat tile id over several problems -> (group, m, n).
 
     Problems are laid out one after another in the flat id (problem g owns the ids
-    from sum_{h<g} tiles_m[h]*nt on), and the same raster map applies inside each.
+    from sum_{h<g} tiles_m[h]*nt[h] on), and the same raster map applies inside each.
+    ``nt`` is one tile-column count for all problems or one per problem.
     """
+    nts = list(nt) if isinstance(nt, (list, tuple)) else [nt] * len(tiles_m)
     base = 0
-    for g, mt in enumerate(tiles_m):
-        cnt = mt * nt
+    for g, (mt, ntg) in enumerate(zip(tiles_m, nts)):
+        cnt = mt * ntg
         if c < base + cnt:
-            m, n = raster(c - base, mt, nt, group_rows)
+            m, n = raster(c - base, mt, ntg, group_rows)
             return g, m, n
         base += cnt
     raise ValueError(f"flat tile id {c} beyond {base} tiles")

@@ -34,10 +34,12 @@ def assert_close(C_gpu, C_ref, rel=1e-3):
 
 def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8):
     """(owner_lin, claims_lin) indexed by linear cluster-tile id, from CTA-tile logs.
-    tiles_m: cluster-tile rows of each problem (one entry for a plain problem)."""
+    tiles_m: cluster-tile rows of each problem (one entry for a plain problem); nt: tile
+    columns, one count for all problems or one per problem."""
     owner_lin, claims_lin = [], []
     base = 0
-    for mt in tiles_m:
+    nts = list(nt) if isinstance(nt, (list, tuple)) else [nt] * len(tiles_m)
+    for mt, nt in zip(tiles_m, nts):
         for c in range(mt * nt):
             m, n = cv.raster(c, mt, nt, group_rows)
             pos = [base * cl + (m * cl + r) * nt + n for r in range(cl)]

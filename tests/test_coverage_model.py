@@ -140,3 +140,13 @@ def test_device_log_checker_accepts_and_rejects():
         cv.check_device_log(cv.CLC, [0, 1, 2, 0, 3, 2], [1] * 6, [0, 1, 2, 3, -1, -1], 6)
     with pytest.raises(AssertionError):   # a worker did not start with its own tile
         cv.check_device_log(cv.CLC, owner, [1] * 6, [0, 1, 3, -1, -1, -1], 6)
+
+
+def test_grouped_tile_per_problem_columns():
+    tiles_m, nts = [2, 1, 3], [1, 3, 2]
+    out = [cv.grouped_tile(c, tiles_m, nts) for c in range(2 + 3 + 6)]
+    assert out[:2] == [(0, 0, 0), (0, 1, 0)]
+    assert out[2:5] == [(1, 0, 0), (1, 0, 1), (1, 0, 2)]
+    assert out[5:] == [(2, 0, 0), (2, 1, 0), (2, 2, 0), (2, 0, 1), (2, 1, 1), (2, 2, 1)]
+    # the same as the uniform form when every problem has the same column count
+    assert [cv.grouped_tile(c, [2, 3], [4, 4]) for c in range(20)] == [cv.grouped_tile(c, [2, 3], 4) for c in range(20)]

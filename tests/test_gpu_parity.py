@@ -303,3 +303,43 @@ def test_run_host_banded_pipeline(g, tile, cl):
     s.synchronize()
     g.sync(s)
     assert_close(Ch.numpy(), oracle.gemm(A, B))
+
+
+@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("mode", MODES)
+def test_grouped_varied_shapes_small(g, tile, cl, mode):
+    """Problems of different M, N and K in one flat grid (ragged edges, an empty problem,
+    a K = 0 problem whose C must be zero)."""
+    shapes = [(300, 520, 192), (128, 256, 1000), (0, 256, 64), (700, 264, 64), (256, 776, 0), (64, 1024, 512)]
+    gen = torch.Generator().manual_seed(73)
+    As = [(torch.rand((m, k), generator=gen) * 2 - 1).to(torch.bfloat16) for m, n, k in shapes]
+    Bs = [(torch.rand((k, n), generator=gen) * 2 - 1).to(torch.bfloat16) for m, n, k in shapes]
+    dC = [torch.full((m, n), float("nan"), device="cuda") for m, n, k in shapes]
+    g.run_grouped_v([a.cuda() for a in As], [b.cuda() for b in Bs], dC, tile=tile, cluster=cl, sched=mode,
+                    num_workers=3)
+    g.sync()
+    for (m, n, k), a, b, c in zip(shapes, As, Bs, dC):
+        if m and n:
+            ref = oracle.gemm(a, b) if k else np.zeros((m, n))
+            assert_close(c.cpu().numpy(), ref)
+    live = [(m, n) for m, n, k in shapes if m and n]
+    check_log(g, mode, [math.ceil(m / (128 * cl)) for m, n in live], [math.ceil(n / tile[1]) for m, n in live], cl,
+              num_workers=3 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_grouped_varied_depth_full_size_sampled(g, mode):
+    """64 problems with K_g = 256 ceil(lognormal(2, 1)) in [256, 16384] and M_g as in the
+    grouped workload (seed 5), N = 4096: tiles of unequal cost in one flat grid."""
+    w = wl.grouped_varied_depth()
+    As, Bs = _inputs(w)
+    dA = [a.cuda() for a in As]
+    dB = [b.cuda() for b in Bs]
+    dC = [torch.full((m, w.N), float("nan"), device="cuda") for m in w.group_m]
+    g.run_grouped_v(dA, dB, dC, sched=mode, num_workers=148)
+    g.sync()
+    rng = np.random.default_rng(5)
+    for a, b, c, m in zip(As, Bs, dC, w.group_m):
+        _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
+                       blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
+    check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)

@@ -11,7 +11,10 @@ Recipe (the pages publish no inputs; every workload is synthetic):
   round-to-nearest-even; "normal" entries are ``torch.randn * sigma`` rounded the same
   way;
 * grouped row counts are ``128 * ceil(x)`` clipped to [128, 8192], with x drawn from
-  ``numpy.random.default_rng(seed).lognormal(mean=2, sigma=1, size=G)``.
+  ``numpy.random.default_rng(seed).lognormal(mean=2, sigma=1, size=G)``;
+* the variable-depth grouped workload draws, from one ``default_rng(5)``, the row counts
+  as above and then depths ``K_g = 256 * ceil(x)`` clipped to [256, 16384] from a second
+  ``lognormal(2, 1, G)`` draw; N = 4096 for every problem.
 """
 from __future__ import annotations
 
@@ -35,20 +38,22 @@ class Workload:
     bn: int = 256
     cluster: int = 1
     group_m: Tuple[int, ...] = field(default_factory=tuple)   # grouped problems only
+    group_k: Tuple[int, ...] = field(default_factory=tuple)   # per-problem depth (else K for all)
+
+    def depths(self) -> Tuple[int, ...]:
+        return self.group_k if self.group_k else (self.K,) * len(self.group_m)
 
     @property
     def flops(self) -> float:
         if self.group_m:
-            return 2.0 * sum(self.group_m) * self.N * self.K
+            return 2.0 * self.N * sum(m * k for m, k in zip(self.group_m, self.depths()))
         return 2.0 * self.M * self.N * self.K
 
     @property
     def min_bytes(self) -> float:
         """Each operand read once and C written once (bf16 in, fp32 out)."""
         if self.group_m:
-            G = len(self.group_m)
-            Ms = sum(self.group_m)
-            return 2.0 * (Ms * self.K + G * self.K * self.N) + 4.0 * Ms * self.N
+            return sum(2.0 * (m * k + k * self.N) + 4.0 * m * self.N for m, k in zip(self.group_m, self.depths()))
         return 2.0 * (self.M * self.K + self.K * self.N) + 4.0 * self.M * self.N
 
 
@@ -76,6 +81,15 @@ def grouped() -> Workload:
     return Workload("grouped_64x(Mg)x4096x4096", sum(gm), 4096, 4096, seed=4, group_m=gm)
 
 
+def grouped_varied_depth(G: int = 64, seed: int = 5) -> Workload:
+    rng = np.random.default_rng(seed)
+    m = np.clip(128 * np.ceil(rng.lognormal(mean=2.0, sigma=1.0, size=G)), 128, 8192).astype(np.int64)
+    k = np.clip(256 * np.ceil(rng.lognormal(mean=2.0, sigma=1.0, size=G)), 256, 16384).astype(np.int64)
+    gm = tuple(int(v) for v in m)
+    gk = tuple(int(v) for v in k)
+    return Workload("grouped_varK_64x(Mg)x4096x(Kg)", sum(gm), 4096, max(gk), seed=seed, group_m=gm, group_k=gk)
+
+
 def _draw(gen: torch.Generator, shape, dist: str, sigma: float) -> torch.Tensor:
     if dist == "uniform":
         x = torch.rand(shape, generator=gen, dtype=torch.float32).mul_(2.0).sub_(1.0)
@@ -97,9 +111,9 @@ def make_inputs(w: Workload, dist: Optional[str] = None, pin: bool = False):
     if w.group_m:
         As: List[torch.Tensor] = []
         Bs: List[torch.Tensor] = []
-        for m in w.group_m:
-            a = _draw(gen, (m, w.K), d, w.sigma)
-            b = _draw(gen, (w.K, w.N), d, w.sigma)
+        for m, k in zip(w.group_m, w.depths()):
+            a = _draw(gen, (m, k), d, w.sigma)
+            b = _draw(gen, (k, w.N), d, w.sigma)
             As.append(a.pin_memory() if pin else a)
             Bs.append(b.pin_memory() if pin else b)
         return As, Bs
