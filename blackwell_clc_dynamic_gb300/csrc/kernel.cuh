@@ -26,13 +26,11 @@ namespace clcg {
 enum : int { SCHED_CLC = 0, SCHED_STATIC = 1, SCHED_NONPERSISTENT = 2 };
 
 constexpr int BM = 128;          // rows of C per CTA
-constexpr int BK = 64;           // k-slice per ring stage (128 bytes of bf16: one swizzle row)
 constexpr int UMMA_K = 16;       // k per tcgen05.mma kind::f16
 constexpr int NUM_THREADS = 256;
 constexpr int CLC_DEPTH = 3;     // response ring depth
 constexpr int THR_DEPTH = 3;     // throttle ring depth
 constexpr int EPI_WARP0 = 4;
-constexpr int EPI_CHUNK = 32;    // fp32 columns per epilogue store
 constexpr int TRACE_WORDS = 8;   // u64 per CTA tile in the optional trace
 
 // Device error word: [0] bits, [1] first failing wait site, [2] block of that wait.
@@ -50,11 +48,11 @@ struct Params {
   const int* g_tile_start;       // grouped: G+1 prefix sums of cluster tiles
   const int* g_mt;               // grouped: cluster-tile rows of each problem
   const int* g_nt;               // grouped: tile columns of each problem
-  const int* g_kb;               // grouped: k-blocks (ceil(K_g / 64)) of each problem
+  const int* g_kb;               // grouped: k-blocks (ceil(K_g / BK)) of each problem
   int G;                         // number of problems (0: plain problem in tmA/tmB/tmC)
   int mt, nt;                    // cluster-tile grid of the plain problem
   int total;                     // cluster tiles in the launch
-  int k_blocks;                  // ceil(K / 64)
+  int k_blocks;                  // ceil(K / BK)
   int raster_group;              // tile rows per raster band
   int* log_owner;                // [CTA tiles] worker that computed the tile (or null)
   int* log_claims;               // [CTA tiles] times the tile was computed
@@ -74,17 +72,27 @@ struct Cfg {
   static constexpr int CL = CL_;                // CTAs per cluster
   static constexpr int BN_CTA = BN / CL;        // B columns each CTA loads
   static constexpr int MMA_M = BM * CL;
+  // The one-CTA 128 x 256 tile needs the most operand bytes per MMA cycle; it takes 32-deep
+  // k-slices so that nine 24 KiB stages (instead of four of 48 KiB) keep more bytes in
+  // flight.  The other shapes take 64-deep slices (128-byte rows of A).
+  static constexpr bool FINE = (CL == 1 && BN == 256);
+  static constexpr int BK = FINE ? 32 : 64;     // k per ring stage
+  static constexpr int A_ROW = BK * 2;          // bytes per A row in a stage (64 or 128)
+  static constexpr int A_SWZ = FINE ? 4 : 2;    // smem descriptor swizzle code: 4 = 64 B, 2 = 128 B
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int B_BOXES = BN_CTA / 64;   // 64-column TMA boxes per stage
-  static constexpr int STAGES = (CL == 1 && BN == 256) ? 4 : 6;
+  static constexpr int STAGES = FINE ? 9 : 6;
   static constexpr int TX_BYTES = (A_BYTES + B_BYTES) * CL;   // counted on the leader's barrier
   static constexpr int TMEM_COLS = 2 * BN;      // two accumulators of BN fp32 columns
-  static constexpr int C_BUF_BYTES = 32 * EPI_CHUNK * 4;
+  static constexpr int EPI_CHUNK = FINE ? 16 : 32;             // fp32 columns per epilogue store
+  static constexpr int C_ROW = EPI_CHUNK * 4;                  // bytes per staged C row (64 or 128)
+  static constexpr int C_BUFS = FINE ? 1 : 2;                  // staging buffers per epilogue warp
+  static constexpr int C_BUF_BYTES = 32 * C_ROW;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_C + 4 * 2 * C_BUF_BYTES;
+  static constexpr int OFF_BAR = OFF_C + 4 * C_BUFS * C_BUF_BYTES;
   // barrier indices
   static constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES,
                        BAR_ACC_EMPTY = 2 * STAGES + 2, BAR_CLC_FULL = 2 * STAGES + 4,
@@ -97,24 +105,47 @@ struct Cfg {
   // consumer warps of a CLC response: TMA + 4 epilogue warps per CTA, MMA + scheduler on rank 0
   static constexpr int CLC_CONSUMERS = 5 * CL + 2;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(BN % EPI_CHUNK == 0 && BN_CTA % 64 == 0, "tile shape");
+  static_assert(BN % EPI_CHUNK == 0 && BN_CTA % 64 == 0 && BK % UMMA_K == 0, "tile shape");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && C_BUF_BYTES % 1024 == 0, "1 KiB alignment");
 };
+
+// Host view of a shape's TMA boxes and k-slice depth.
+struct ShapeInfo {
+  int bk;          // k per stage (A box width, B box height)
+  int epi_chunk;   // C box width (fp32 columns)
+  int a_swizzle;   // bytes: 64 or 128
+  int c_swizzle;   // bytes: 64 or 128
+  int smem;
+};
+
+template <int BN, int CL>
+constexpr ShapeInfo shape_info_of() {
+  using C = Cfg<BN, CL>;
+  return ShapeInfo{C::BK, C::EPI_CHUNK, C::A_ROW, C::C_ROW, C::SMEM_BYTES};
+}
+
+inline ShapeInfo shape_info(int bn, int cl) {
+  if (cl == 2) return shape_info_of<256, 2>();
+  return bn == 128 ? shape_info_of<128, 1>() : shape_info_of<256, 1>();
+}
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05): start >> 4 in [0,14), leading byte offset >> 4
 // in [16,30), stride byte offset >> 4 in [32,46), fixed 0b001 in [46,49), base offset 0,
-// swizzle mode in [61,64) with 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// swizzle mode in [61,64): 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+         ((uint64_t)1 << 46) | ((uint64_t)swz << 61);
 }
 
-// A tile, K-major: rows of 64 bf16 (128 B), 8-row swizzle atoms 1024 B apart.
-__device__ __forceinline__ uint64_t desc_a(uint32_t addr) { return smem_desc(addr, 16, 1024); }
+// A tile, K-major: rows of BK bf16 (A_ROW bytes), 8-row swizzle atoms 8 * A_ROW bytes apart.
+template <class C>
+__device__ __forceinline__ uint64_t desc_a(uint32_t addr) { return smem_desc(addr, 16, 8 * C::A_ROW, C::A_SWZ); }
 
-// B tile, MN-major: 64-column (128 B) atoms of 64 k-rows (8 KiB apart along n), 8 k-rows
-// per swizzle atom (1024 B apart along k).
-__device__ __forceinline__ uint64_t desc_b(uint32_t addr) { return smem_desc(addr, BK * 128, 1024); }
+// B tile, MN-major: 64-column (128 B) atoms of BK k-rows (BK * 128 B apart along n), 8
+// k-rows per 128-byte swizzle atom (1024 B apart along k).
+template <class C>
+__device__ __forceinline__ uint64_t desc_b(uint32_t addr) { return smem_desc(addr, C::BK * 128, 1024, 2); }
 
 // Instruction descriptor, kind::f16: D f32 (bit 4), A bf16 (bits 7-9 = 1), B bf16 (bits 10-12
 // = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 at bit 17, M >> 4 at bit 24.
@@ -336,9 +367,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const int bx = w.n_blk * BN + (int)rank * C::BN_CTA;
         const int pf = p.l2_prefetch;
         auto prefetch = [&](int kq) {
-          tma_prefetch_l2_2d(mA, kq * BK, ay);
+          tma_prefetch_l2_2d(mA, kq * C::BK, ay);
 #pragma unroll
-          for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_l2_2d(mB, bx + 64 * j, kq * BK);
+          for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_l2_2d(mB, bx + 64 * j, kq * C::BK);
         };
         for (int kq = C::STAGES; kq < pf && kq < w.kb; ++kq) prefetch(kq);
         bool ok = true;
@@ -350,15 +381,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           const uint32_t b_dst = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
           if constexpr (CL == 1) {
             const uint32_t fb = bar(C::BAR_FULL + s);
-            tma_load_2d(a_dst, mA, fb, kb * BK, ay);
-#pragma unroll
-            for (int j = 0; j < C::B_BOXES; ++j) tma_load_2d(b_dst + j * BK * 128, mB, fb, bx + 64 * j, kb * BK);
-          } else {
-            const uint32_t fb = full0_leader + 8u * (uint32_t)s;
-            tma_load_2d_pair(a_dst, mA, fb, kb * BK, ay);
+            tma_load_2d(a_dst, mA, fb, kb * C::BK, ay);
 #pragma unroll
             for (int j = 0; j < C::B_BOXES; ++j)
-              tma_load_2d_pair(b_dst + j * BK * 128, mB, fb, bx + 64 * j, kb * BK);
+              tma_load_2d(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
+          } else {
+            const uint32_t fb = full0_leader + 8u * (uint32_t)s;
+            tma_load_2d_pair(a_dst, mA, fb, kb * C::BK, ay);
+#pragma unroll
+            for (int j = 0; j < C::B_BOXES; ++j)
+              tma_load_2d_pair(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
           }
           if (++s == C::STAGES) { s = 0; ph ^= 1; }
         }
@@ -391,8 +423,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           const uint32_t a_addr = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
           const uint32_t b_addr = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            mma_bf16<CL>(d, desc_a(a_addr + kk * UMMA_K * 2), desc_b(b_addr + kk * UMMA_K * 128), idesc,
+          for (int kk = 0; kk < C::BK / UMMA_K; ++kk)
+            mma_bf16<CL>(d, desc_a<C>(a_addr + kk * UMMA_K * 2), desc_b<C>(b_addr + kk * UMMA_K * 128), idesc,
                          (kb | kk) != 0);
           if constexpr (CL == 1) mma_commit(bar(C::BAR_EMPTY + s));
           else mma_commit_pair(bar(C::BAR_EMPTY + s), 0x3);
@@ -466,7 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     int acc = 0;
     uint32_t aph = 0;
     bool first_tile = true;
-    const uint32_t cbuf = sb + C::OFF_C + (uint32_t)q * 2u * C::C_BUF_BYTES;
+    const uint32_t cbuf = sb + C::OFF_C + (uint32_t)q * (uint32_t)C::C_BUFS * C::C_BUF_BYTES;
     const uint32_t acc_empty_leader0 =
         (CL == 1) ? bar(C::BAR_ACC_EMPTY) : map_to_rank(bar(C::BAR_ACC_EMPTY), 0);
     int chunk_seq = 0;
@@ -476,11 +508,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       const CUtensorMap* mC = p.G ? p.gmaps + 3 * w.g + 2 : &p.tmC;
       const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int ch = 0; ch < BN / EPI_CHUNK; ++ch) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tcol + (uint32_t)(ch * EPI_CHUNK), v);
+      for (int ch = 0; ch < BN / C::EPI_CHUNK; ++ch) {
+        uint32_t v[C::EPI_CHUNK];
+        if constexpr (C::EPI_CHUNK == 32) tmem_ld_32x32b_x32(tcol + (uint32_t)(ch * C::EPI_CHUNK), v);
+        else tmem_ld_32x32b_x16(tcol + (uint32_t)(ch * C::EPI_CHUNK), v);
         tmem_wait_ld();
-        if (ch == BN / EPI_CHUNK - 1) {
+        if (ch == BN / C::EPI_CHUNK - 1) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
@@ -491,15 +524,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
         if (w.kb == 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0u;
+          for (int j = 0; j < C::EPI_CHUNK; ++j) v[j] = 0u;
         }
-        const uint32_t buf = cbuf + (uint32_t)(chunk_seq & 1) * C::C_BUF_BYTES;
-        if (lane == 0) bulk_wait_group_read<1>();   // the store that last used `buf` has read it
+        const uint32_t buf = cbuf + (uint32_t)(chunk_seq % C::C_BUFS) * C::C_BUF_BYTES;
+        // the store that last used `buf` has finished reading it
+        if (lane == 0) bulk_wait_group_read<C::C_BUFS - 1>();
         __syncwarp();
-        const uint32_t row = buf + lane * 128u;
+        // row `lane` of the box; TMA swizzle: 16-byte chunk j of a 128-byte row sits at
+        // j ^ (row % 8), of a 64-byte row at j ^ ((row / 2) % 4)
+        const uint32_t row = buf + lane * (uint32_t)C::C_ROW;
+        const uint32_t xr = (C::C_ROW == 128) ? (lane & 7u) : ((lane >> 1) & 3u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t dst = row + ((uint32_t)(j ^ (int)(lane & 7)) << 4);
+        for (int j = 0; j < C::C_ROW / 16; ++j) {
+          const uint32_t dst = row + (((uint32_t)j ^ xr) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[4 * j]), "r"(v[4 * j + 1]),
                        "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
                        : "memory");
@@ -507,7 +544,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(mC, buf, w.n_blk * BN + ch * EPI_CHUNK, w.m_blk * BM + q * 32);
+          tma_store_2d(mC, buf, w.n_blk * BN + ch * C::EPI_CHUNK, w.m_blk * BM + q * 32);
           bulk_commit_group();
         }
         ++chunk_seq;

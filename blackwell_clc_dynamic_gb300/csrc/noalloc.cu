@@ -83,14 +83,14 @@ int setup_device(int dev) {
 }
 
 int encode(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
-           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+           uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle swz = swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
 }
 
@@ -150,19 +150,23 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   Params p;
   memset(&p, 0, sizeof p);
+  const ShapeInfo si = shape_info(bn, cl);
   if (K > 0) {
-    rc = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, BK, BM);
+    rc = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
+                (uint32_t)si.bk, BM, si.a_swizzle);
     if (rc) return rc;
-    rc = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64, BK);
+    rc = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64,
+                (uint32_t)si.bk, 128);
     if (rc) return rc;
   }
-  rc = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 4, EPI_CHUNK, 32);
+  rc = encode(&p.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, (uint64_t)N, (uint64_t)M, (uint64_t)N * 4,
+              (uint32_t)si.epi_chunk, 32, si.c_swizzle);
   if (rc) return rc;
   p.G = 0;
   p.mt = (int)mt;
   p.nt = (int)nt;
   p.total = (int)total;
-  p.k_blocks = (int)((K + BK - 1) / BK);
+  p.k_blocks = (int)((K + si.bk - 1) / si.bk);
   p.raster_group = 8;
   p.log_owner = owner;
   p.log_claims = claims;

@@ -76,7 +76,9 @@ typedef enum {
 
 /* Output tile per cluster.  Supported: {128, 256, 64} and {128, 128, 64} with cluster
  * {1,1,1}; {128, 256, 64} with cluster {2,1,1}, where the pair computes a 256 x 256
- * tile (each CTA 128 x 256) with a CTA-pair MMA. */
+ * tile (each CTA 128 x 256) with a CTA-pair MMA.  bk must be 64; the library picks the k
+ * depth of its shared-memory ring stages (32 for the one-CTA 128 x 256 tile, which keeps
+ * nine stages in flight, 64 otherwise). */
 typedef struct { int bm, bn, bk; } gemm_tile_t;
 typedef struct { int x, y, z; } gemm_cluster_t;
 
