@@ -342,8 +342,7 @@ def run_ours(args, ws, rank, local):
             total_ms, per = time_steps(step(mode, nw), args.steps, args.warmup, stream, barrier, sync_all)
             if sampler:
                 clocks = sampler.stop()
-            total_ms = max_over_ranks(total_ms, ws)
-            tflops = ws * args.steps * w.flops / (total_ms * 1e-3) / 1e12
+            tflops, total_ms = job_throughput(total_ms, args.steps, w.flops, ws)
             modes[key] = {"tflops": tflops, "ms_per_step": total_ms / args.steps,
                           "ms_min": min(per), "ms_median": statistics.median(per), "ms_max": max(per),
                           "pct_bf16_peak_burst": 100.0 * tflops / ws / peaks["bf16_tflops"],
@@ -428,13 +427,23 @@ def run_ours(args, ws, rank, local):
 
 
 def max_over_ranks(x, ws):
+    """The slowest rank's value (replicas are timed independently; the job takes as long
+    as its slowest replica)."""
     if ws <= 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(total_ms_local, steps, flops_per_step, ws):
+    """Whole-job TFLOP/s of ws replicas: every rank runs `steps` steps of `flops_per_step`;
+    the time is the slowest rank's (weak scaling)."""
+    t = max_over_ranks(total_ms_local, ws)
+    return ws * steps * flops_per_step / (t * 1e-3) / 1e12, t
 
 
 # ------------------------------------------------------------------ --all: the other workloads
