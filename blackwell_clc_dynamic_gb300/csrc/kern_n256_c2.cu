@@ -1,9 +1,9 @@
-// Kernel instantiations for tile N = 256, cluster = 2 CTA(s).
+// Kernel instantiations for tile N = 256, cluster of 2 CTA(s), CTA-pair MMA
 #include "launch.cuh"
 
 namespace clcg {
 cudaError_t launch_n256_c2(int sched, const Params& p, int grid_ctas, cudaStream_t stream) {
-  return launch_shape<256, 2>(sched, p, grid_ctas, stream);
+  return launch_shape<256, 2, true>(sched, p, grid_ctas, stream);
 }
-cudaError_t max_clusters_n256_c2(int* out) { return max_clusters_shape<256, 2>(out); }
+cudaError_t max_clusters_n256_c2(int* out) { return max_clusters_shape<256, 2, true>(out); }
 }  // namespace clcg

@@ -66,24 +66,38 @@ struct Params {
   int hold_scheduler;            // test hook: the CLC scheduler issues and signals nothing
 };
 
-template <int BN_, int CL_>
+// Cluster shapes:
+//   CL == 1            one CTA, one 128 x BN tile
+//   CL == 2, PAIR      a CTA pair runs one tcgen05 cta_group::2 MMA of 256 x BN; each CTA
+//                      loads its own 128 rows of A and its own BN/2 columns of B
+//   CL == 2 or 4, !PAIR  CL CTAs each run their own 128 x BN MMA on consecutive row blocks
+//                      and share the B tile: each loads 1/CL of it and multicasts that part
+//                      to every CTA of the cluster
+template <int BN_, int CL_, bool PAIR_>
 struct Cfg {
   static constexpr int BN = BN_;                // columns of C per cluster tile (MMA N)
   static constexpr int CL = CL_;                // CTAs per cluster
-  static constexpr int BN_CTA = BN / CL;        // B columns each CTA loads
-  static constexpr int MMA_M = BM * CL;
-  // The one-CTA 128 x 256 tile needs the most operand bytes per MMA cycle; it takes 32-deep
+  static constexpr bool PAIR = PAIR_;
+  static constexpr bool MCAST = (CL > 1 && !PAIR);
+  static constexpr int CG = PAIR ? 2 : 1;       // tcgen05 cta_group
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns each CTA holds in shared memory
+  static constexpr int MMA_M = PAIR ? 2 * BM : BM;
+  // The 128 x 256 per-CTA MMA needs the most operand bytes per MMA cycle; it takes 32-deep
   // k-slices so that nine 24 KiB stages (instead of four of 48 KiB) keep more bytes in
   // flight.  The other shapes take 64-deep slices (128-byte rows of A).
-  static constexpr bool FINE = (CL == 1 && BN == 256);
+  static constexpr bool FINE = (!PAIR && BN == 256);
   static constexpr int BK = FINE ? 32 : 64;     // k per ring stage
   static constexpr int A_ROW = BK * 2;          // bytes per A row in a stage (64 or 128)
   static constexpr int A_SWZ = FINE ? 4 : 2;    // smem descriptor swizzle code: 4 = 64 B, 2 = 128 B
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int B_BOXES = BN_CTA / 64;   // 64-column TMA boxes per stage
+  static constexpr int B_OWN_BOXES = MCAST ? B_BOXES / CL : B_BOXES;   // boxes this CTA loads
   static constexpr int STAGES = FINE ? 9 : 6;
-  static constexpr int TX_BYTES = (A_BYTES + B_BYTES) * CL;   // counted on the leader's barrier
+  // transaction bytes on the full barrier the MMA waits on: the pair's leader counts both
+  // CTAs' loads; a multicast CTA receives its A and the whole B tile
+  static constexpr int TX_BYTES = PAIR ? (A_BYTES + B_BYTES) * 2 : (A_BYTES + B_BYTES);
+  static constexpr int EMPTY_ARRIVALS = MCAST ? CL : 1;   // MMA commits that free a stage
   static constexpr int TMEM_COLS = 2 * BN;      // two accumulators of BN fp32 columns
   static constexpr int EPI_CHUNK = FINE ? 16 : 32;             // fp32 columns per epilogue store
   static constexpr int C_ROW = EPI_CHUNK * 4;                  // bytes per staged C row (64 or 128)
@@ -102,10 +116,13 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_RESP + CLC_DEPTH * 16;   // [0] tmem base [1] abort [2..4] injected
   static constexpr int SMEM_USED = OFF_MISC + 32;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;         // slack to align the base to 1 KiB
-  // consumer warps of a CLC response: TMA + 4 epilogue warps per CTA, MMA + scheduler on rank 0
-  static constexpr int CLC_CONSUMERS = 5 * CL + 2;
+  // consumer warps of a CLC response: TMA + 4 epilogue warps in every CTA, the MMA warp of
+  // every CTA that issues MMAs, and the scheduler warp of rank 0
+  static constexpr int CLC_CONSUMERS = 5 * CL + (PAIR ? 1 : CL) + 1;
+  static_assert(!PAIR || CL == 2, "CTA pairs only");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % EPI_CHUNK == 0 && BN_CTA % 64 == 0 && BK % UMMA_K == 0, "tile shape");
+  static_assert(B_BOXES % (MCAST ? CL : 1) == 0, "B boxes split evenly over the cluster");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && C_BUF_BYTES % 1024 == 0, "1 KiB alignment");
 };
 
@@ -118,15 +135,17 @@ struct ShapeInfo {
   int smem;
 };
 
-template <int BN, int CL>
+template <int BN, int CL, bool PAIR>
 constexpr ShapeInfo shape_info_of() {
-  using C = Cfg<BN, CL>;
+  using C = Cfg<BN, CL, PAIR>;
   return ShapeInfo{C::BK, C::EPI_CHUNK, C::A_ROW, C::C_ROW, C::SMEM_BYTES};
 }
 
-inline ShapeInfo shape_info(int bn, int cl) {
-  if (cl == 2) return shape_info_of<256, 2>();
-  return bn == 128 ? shape_info_of<128, 1>() : shape_info_of<256, 1>();
+inline ShapeInfo shape_info(int bn, int cl, bool pair) {
+  if (cl == 2 && pair) return shape_info_of<256, 2, true>();
+  if (cl == 2) return shape_info_of<256, 2, false>();
+  if (cl == 4) return shape_info_of<256, 4, false>();
+  return bn == 128 ? shape_info_of<128, 1, false>() : shape_info_of<256, 1, false>();
 }
 
 // ---------------------------------------------------------------- descriptors
@@ -245,7 +264,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const Pa
 // ---------------------------------------------------------------- work iterator
 // Every role walks the same tile sequence.  In CLC mode each role consumes every response
 // of the ring (one release per consuming warp).
-template <int BN, int CL, int SCHED>
+template <int BN, int CL, bool PAIR, int SCHED>
 struct WorkIter {
   int c = 0;
   int stage = 0;
@@ -259,7 +278,7 @@ struct WorkIter {
   // `warp_wide`: all 32 lanes call (one release per warp); otherwise a single lane calls.
   __device__ __forceinline__ Work next(const Params& p, uint32_t rank, uint32_t smem_base, Ctl ctl,
                                        bool warp_wide) {
-    using C = Cfg<BN, CL>;
+    using C = Cfg<BN, CL, PAIR>;
     if constexpr (SCHED == SCHED_STATIC) {
       c += (int)(gridDim.x / CL);
       return make_work<CL>(p, c, rank);
@@ -293,9 +312,9 @@ struct WorkIter {
 };
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, int CL, int SCHED>
+template <int BN, int CL, bool PAIR, int SCHED>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<BN, CL>;
+  using C = Cfg<BN, CL, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -313,11 +332,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::BAR_FULL + s), 1);
-      mbar_init(bar(C::BAR_EMPTY + s), 1);
+      mbar_init(bar(C::BAR_EMPTY + s), C::EMPTY_ARRIVALS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(C::BAR_ACC_FULL + a), 1);
-      mbar_init(bar(C::BAR_ACC_EMPTY + a), 4 * CL);
+      mbar_init(bar(C::BAR_ACC_EMPTY + a), PAIR ? 8 : 4);
     }
     for (int i = 0; i < CLC_DEPTH; ++i) {
       mbar_init(bar(C::BAR_CLC_FULL + i), 1);
@@ -336,8 +355,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     prefetch_tmap(&p.tmC);
   }
   if (warp == 1) {
-    tmem_alloc<CL>(smem_addr((const void*)(smem + C::OFF_MISC)), C::TMEM_COLS);
-    tmem_relinquish<CL>();
+    tmem_alloc<C::CG>(smem_addr((const void*)(smem + C::OFF_MISC)), C::TMEM_COLS);
+    tmem_relinquish<C::CG>();
   }
   tc_fence_before();
   if constexpr (CL > 1) cluster_sync(); else __syncthreads();
@@ -347,12 +366,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
-      WorkIter<BN, CL, SCHED> it;
+      WorkIter<BN, CL, PAIR, SCHED> it;
       Work w = it.first(p, rank);
       int s = 0;
       uint32_t ph = 0;
       int tile = 0;
-      const uint32_t full0_leader = (CL == 1) ? bar(C::BAR_FULL) : map_to_rank(bar(C::BAR_FULL), 0);
+      const uint32_t full0_leader = PAIR ? map_to_rank(bar(C::BAR_FULL), 0) : bar(C::BAR_FULL);
+      constexpr uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
       while (w.valid) {
         if (SCHED == SCHED_CLC && rank == 0) {
           // throttle: one token per tile started; the scheduler fetches only after it
@@ -364,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;
         const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
         const int ay = w.m_blk * BM;
-        const int bx = w.n_blk * BN + (int)rank * C::BN_CTA;
+        const int bx = w.n_blk * BN + (PAIR ? (int)rank * C::BN_CTA : 0);
         const int pf = p.l2_prefetch;
         auto prefetch = [&](int kq) {
           tma_prefetch_l2_2d(mA, kq * C::BK, ay);
@@ -375,22 +395,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         bool ok = true;
         for (int kb = 0; kb < w.kb; ++kb) {
           if (pf > 0 && kb + pf < w.kb && kb + pf >= C::STAGES) prefetch(kb + pf);
-          if (!bar_wait(bar(C::BAR_EMPTY + s), ph ^ 1, p, ctl, WAIT_EMPTY)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TX_BYTES);
+          if (!bar_wait<(CL > 1)>(bar(C::BAR_EMPTY + s), ph ^ 1, p, ctl, WAIT_EMPTY)) { ok = false; break; }
+          if (!PAIR || rank == 0) mbar_arrive_expect_tx(bar(C::BAR_FULL + s), C::TX_BYTES);
           const uint32_t a_dst = sb + C::OFF_A + (uint32_t)s * C::A_BYTES;
           const uint32_t b_dst = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
-          if constexpr (CL == 1) {
-            const uint32_t fb = bar(C::BAR_FULL + s);
-            tma_load_2d(a_dst, mA, fb, kb * C::BK, ay);
-#pragma unroll
-            for (int j = 0; j < C::B_BOXES; ++j)
-              tma_load_2d(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
-          } else {
+          if constexpr (PAIR) {
             const uint32_t fb = full0_leader + 8u * (uint32_t)s;
             tma_load_2d_pair(a_dst, mA, fb, kb * C::BK, ay);
 #pragma unroll
             for (int j = 0; j < C::B_BOXES; ++j)
               tma_load_2d_pair(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
+          } else {
+            const uint32_t fb = bar(C::BAR_FULL + s);
+            tma_load_2d(a_dst, mA, fb, kb * C::BK, ay);
+#pragma unroll
+            for (int i = 0; i < C::B_OWN_BOXES; ++i) {
+              const int j = (int)rank * C::B_OWN_BOXES + i;   // this CTA's share of the B tile
+              if constexpr (C::MCAST)
+                tma_load_2d_multicast(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK, all_ctas);
+              else
+                tma_load_2d(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
+            }
           }
           if (++s == C::STAGES) { s = 0; ph ^= 1; }
         }
@@ -404,16 +429,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (rank == 0 && elect_one()) {
-      WorkIter<BN, CL, SCHED> it;
+    if ((!PAIR || rank == 0) && elect_one()) {
+      WorkIter<BN, CL, PAIR, SCHED> it;
       Work w = it.first(p, rank);
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
       constexpr uint32_t idesc = make_idesc<C::MMA_M, BN>();
+      constexpr uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
       while (w.valid) {
-        if (!bar_wait<(CL > 1)>(bar(C::BAR_ACC_EMPTY + acc), aph ^ 1, p, ctl, WAIT_ACC_EMPTY)) break;
+        if (!bar_wait<PAIR>(bar(C::BAR_ACC_EMPTY + acc), aph ^ 1, p, ctl, WAIT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
@@ -424,15 +450,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           const uint32_t b_addr = sb + C::OFF_B + (uint32_t)s * C::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / UMMA_K; ++kk)
-            mma_bf16<CL>(d, desc_a<C>(a_addr + kk * UMMA_K * 2), desc_b<C>(b_addr + kk * UMMA_K * 128), idesc,
-                         (kb | kk) != 0);
-          if constexpr (CL == 1) mma_commit(bar(C::BAR_EMPTY + s));
-          else mma_commit_pair(bar(C::BAR_EMPTY + s), 0x3);
+            mma_bf16<C::CG>(d, desc_a<C>(a_addr + kk * UMMA_K * 2), desc_b<C>(b_addr + kk * UMMA_K * 128), idesc,
+                            (kb | kk) != 0);
+          // the stage is free once these MMAs have read it: in every CTA that shares it
+          if constexpr (PAIR) mma_commit_pair(bar(C::BAR_EMPTY + s), 0x3);
+          else if constexpr (C::MCAST) mma_commit_multicast(bar(C::BAR_EMPTY + s), all_ctas);
+          else mma_commit(bar(C::BAR_EMPTY + s));
           if (++s == C::STAGES) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
-        if constexpr (CL == 1) mma_commit(bar(C::BAR_ACC_FULL + acc));
-        else mma_commit_pair(bar(C::BAR_ACC_FULL + acc), 0x3);
+        if constexpr (PAIR) mma_commit_pair(bar(C::BAR_ACC_FULL + acc), 0x3);
+        else mma_commit(bar(C::BAR_ACC_FULL + acc));
         acc ^= 1;
         if (acc == 0) aph ^= 1;
         w = it.next(p, rank, sb, ctl, false);
@@ -460,17 +488,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if constexpr (CL == 1) {
             clc_try_cancel(resp, full);
           } else {
-            mbar_arrive_expect_tx_cluster(map_to_rank(full, 1), 16);
+            // every CTA of the cluster receives the response at the same offset
+#pragma unroll
+            for (uint32_t r = 1; r < (uint32_t)CL; ++r) mbar_arrive_expect_tx_cluster(map_to_rank(full, r), 16);
             clc_try_cancel_all(resp, full);
           }
         } else {
           // test hook: report a failed fetch without issuing a cancel
           misc[2 + s] = 1;
           mbar_arrive(full);
-          if constexpr (CL > 1) {
-            const uint32_t peer_flag = map_to_rank(smem_addr((const void*)(misc + 2 + s)), 1);
+#pragma unroll
+          for (uint32_t r = 1; r < (uint32_t)CL; ++r) {
+            const uint32_t peer_flag = map_to_rank(smem_addr((const void*)(misc + 2 + s)), r);
             asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_flag), "r"(1u) : "memory");
-            mbar_arrive_cluster(map_to_rank(full, 1));
+            mbar_arrive_cluster(map_to_rank(full, r));
           }
         }
         // the scheduler consumes the response too: it stops at the first failure
@@ -493,14 +524,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - EPI_WARP0;   // TMEM lane quadrant (warp % 4)
-    WorkIter<BN, CL, SCHED> it;
+    WorkIter<BN, CL, PAIR, SCHED> it;
     Work w = it.first(p, rank);
     int acc = 0;
     uint32_t aph = 0;
     bool first_tile = true;
     const uint32_t cbuf = sb + C::OFF_C + (uint32_t)q * (uint32_t)C::C_BUFS * C::C_BUF_BYTES;
-    const uint32_t acc_empty_leader0 =
-        (CL == 1) ? bar(C::BAR_ACC_EMPTY) : map_to_rank(bar(C::BAR_ACC_EMPTY), 0);
+    const uint32_t acc_empty_leader0 = PAIR ? map_to_rank(bar(C::BAR_ACC_EMPTY), 0) : bar(C::BAR_ACC_EMPTY);
     int chunk_seq = 0;
     while (w.valid) {
       if (!bar_wait(bar(C::BAR_ACC_FULL + acc), aph, p, ctl, WAIT_ACC_FULL)) break;
@@ -518,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if (CL == 1) mbar_arrive(bar(C::BAR_ACC_EMPTY + acc));
+            if (!PAIR) mbar_arrive(bar(C::BAR_ACC_EMPTY + acc));
             else mbar_arrive_cluster(acc_empty_leader0 + 8u * (uint32_t)acc);
           }
         }
@@ -575,7 +605,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if constexpr (CL > 1) cluster_sync(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<CL>(tmem_base, C::TMEM_COLS);
+    tmem_dealloc<C::CG>(tmem_base, C::TMEM_COLS);
   }
 }
 

@@ -105,12 +105,14 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     return GEMM_ERR_INVALID_ARG;
   if (tile.bm != 128 || tile.bk != 64 || cluster.y != 1 || cluster.z != 1) return GEMM_ERR_INVALID_ARG;
   int bn = 0, cl = 0;
+  bool pair = false;   // clusters of 2 run the CTA-pair MMA (the default options)
   if (cluster.x == 1 && (tile.bn == 128 || tile.bn == 256)) {
     bn = tile.bn;
     cl = 1;
-  } else if (cluster.x == 2 && tile.bn == 256) {
+  } else if ((cluster.x == 2 || cluster.x == 4) && tile.bn == 256) {
     bn = 256;
-    cl = 2;
+    cl = cluster.x;
+    pair = (cl == 2);
   } else {
     return GEMM_ERR_INVALID_ARG;
   }
@@ -150,7 +152,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   Params p;
   memset(&p, 0, sizeof p);
-  const ShapeInfo si = shape_info(bn, cl);
+  const ShapeInfo si = shape_info(bn, cl, pair);
   if (K > 0) {
     rc = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
                 (uint32_t)si.bk, BM, si.a_swizzle);
@@ -177,9 +179,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   p.inject_fail_after = -1;
 
   const int grid = (int)(workers * cl);
-  if (cl == 2) e = launch_n256_c2((int)sched, p, grid, s);
-  else if (bn == 128) e = launch_n128_c1((int)sched, p, grid, s);
-  else e = launch_n256_c1((int)sched, p, grid, s);
+  e = launch_any(bn, cl, pair, (int)sched, p, grid, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

@@ -74,11 +74,15 @@ typedef enum {
     GEMM_SCHED_NONPERSISTENT = 2
 } gemm_sched_t;
 
-/* Output tile per cluster.  Supported: {128, 256, 64} and {128, 128, 64} with cluster
- * {1,1,1}; {128, 256, 64} with cluster {2,1,1}, where the pair computes a 256 x 256
- * tile (each CTA 128 x 256) with a CTA-pair MMA.  bk must be 64; the library picks the k
- * depth of its shared-memory ring stages (32 for the one-CTA 128 x 256 tile, which keeps
- * nine stages in flight, 64 otherwise). */
+/* Output tile per CTA and cluster shape.  Supported: {128, 256, 64} and {128, 128, 64} with
+ * cluster {1,1,1}; {128, 256, 64} with cluster {2,1,1} (a 256 x 256 tile per cluster,
+ * computed by a CTA-pair MMA, or with gemm_opts_t.cluster_b_multicast by two 128 x 256
+ * MMAs sharing B) and with cluster {4,1,1} (a 512 x 256 tile per cluster: four CTAs on
+ * consecutive row blocks, each loading a quarter of the B tile and multicasting it to
+ * the others).  A successful cancel takes a whole cluster; CTA rank r computes row block
+ * r of the cluster tile.  bk must be 64; the library picks the k depth of its ring stages
+ * (32 when a CTA runs its own 128 x 256 MMA, which keeps nine stages in flight, 64
+ * otherwise). */
 typedef struct { int bm, bn, bk; } gemm_tile_t;
 typedef struct { int x, y, z; } gemm_cluster_t;
 
@@ -96,6 +100,9 @@ typedef struct {
                                   cancel and signals nothing, so every response wait runs out
                                   after timeout_ns; each worker computes its own tile and
                                   gemm_sync reports GEMM_ERR_TIMEOUT */
+    int     cluster_b_multicast; /* clusters of 2: 0 (default) = CTA-pair MMA; 1 = each CTA runs
+                                  its own 128 x 256 MMA and the pair shares the B tile by TMA
+                                  multicast (clusters of 4 always work this way) */
 } gemm_opts_t;
 
 /* Description of the last launch, filled by gemm_last_launch(). */

@@ -19,13 +19,13 @@ pytestmark = pytest.mark.gpu
 WAIT_CLC_FULL = 5
 
 
-@pytest.mark.parametrize("cl", [1, 2], ids=["c1", "c2"])
-def test_response_wait_times_out_and_is_reported(cl):
+@pytest.mark.parametrize("cl,mc", [(1, 0), (2, 0), (4, 0)], ids=["c1", "c2pair", "c4mc"])
+def test_response_wait_times_out_and_is_reported(cl, mc):
     import blackwell_clc_dynamic_gb300 as m
     M, N, K = 128 * cl * 6, 512, 256
     A = wl.make_matrix((M, K), 101)
     B = wl.make_matrix((K, N), 102)
-    with m.Gemm(0, timeout_ns=50_000_000, hold_scheduler=True) as g:
+    with m.Gemm(0, timeout_ns=50_000_000, hold_scheduler=True, cluster_b_multicast=mc) as g:
         C = torch.full((M, N), float("nan"), device="cuda")
         g.run(A.cuda(), B.cuda(), C, tile=TILE_256, cluster=cl, sched="clc")
         torch.cuda.synchronize()

@@ -14,8 +14,9 @@ from tests.gpu_helpers import TILE_128, TILE_256, assert_close, check_log, clust
 pytestmark = pytest.mark.gpu
 
 MODES = ["clc", "static", "nonpersistent"]
-SHAPES = [(TILE_256, 1), (TILE_128, 1), (TILE_256, 2)]
-SHAPE_IDS = ["n256c1", "n128c1", "n256c2"]
+# (tile, cluster size, B multicast): one CTA; CTA pair; clusters of 2 and 4 sharing B
+SHAPES = [(TILE_256, 1, 0), (TILE_128, 1, 0), (TILE_256, 2, 0), (TILE_256, 2, 1), (TILE_256, 4, 0)]
+SHAPE_IDS = ["n256c1", "n128c1", "n256c2", "n256c2mc", "n256c4mc"]
 
 
 @pytest.fixture(scope="module")
@@ -24,6 +25,15 @@ def g():
     h = m.Gemm(0)
     yield h
     h.close()
+
+
+@pytest.fixture
+def mc(g, request):
+    """Selects B multicast for clusters of 2 for one test (from the `shape` parameter)."""
+    flag = request.param
+    g.set_opts(cluster_b_multicast=flag)
+    yield flag
+    g.set_opts(cluster_b_multicast=0)
 
 
 def test_tiny_config_clc(g):
@@ -39,9 +49,9 @@ def test_tiny_config_clc(g):
     check_log(g, "clc", [3], 4, 1)
 
 
-@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("tile,cl,mc", SHAPES, ids=SHAPE_IDS, indirect=["mc"])
 @pytest.mark.parametrize("mode", MODES)
-def test_integer_inputs_bit_exact(g, tile, cl, mode):
+def test_integer_inputs_bit_exact(g, tile, cl, mc, mode):
     """Integer entries in [-4, 4]: every fp32 partial sum is an exact integer below 2^24,
     so any accumulation order must reproduce the oracle bit for bit."""
     M, N, K = 512, 768, 1024
@@ -52,9 +62,9 @@ def test_integer_inputs_bit_exact(g, tile, cl, mode):
     assert np.array_equal(C.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("tile,cl,mc", SHAPES, ids=SHAPE_IDS, indirect=["mc"])
 @pytest.mark.parametrize("mode", MODES)
-def test_uniform_ragged_tail(g, tile, cl, mode):
+def test_uniform_ragged_tail(g, tile, cl, mc, mode):
     """Several tiles in each direction plus ragged M, N and K edges."""
     M, N, K = 1000, 776, 1000
     A = wl.make_matrix((M, K), 21)
@@ -174,8 +184,8 @@ def test_tail_sweep_sampled(g, T):
         check_log(g, mode, [T], 1, 1, num_workers=148 if mode == "static" else None)
 
 
-@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
-def test_grouped_small(g, tile, cl):
+@pytest.mark.parametrize("tile,cl,mc", SHAPES, ids=SHAPE_IDS, indirect=["mc"])
+def test_grouped_small(g, tile, cl, mc):
     """Grouped flat grid over problems of uneven height (including an empty one)."""
     Ms = [128, 300, 0, 1024, 64]
     N, K = 512, 384
@@ -289,8 +299,8 @@ def test_grouped_full_size_sampled(g, mode):
     check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
 
 
-@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
-def test_run_host_banded_pipeline(g, tile, cl):
+@pytest.mark.parametrize("tile,cl,mc", SHAPES, ids=SHAPE_IDS, indirect=["mc"])
+def test_run_host_banded_pipeline(g, tile, cl, mc):
     """gemm_run_host splits the product into blocks (2 row bands x 2 column bands here, the
     last of each ragged), copies them with strided copies and overlaps the copies with the
     block GEMMs on several streams; the result must equal the oracle."""
@@ -305,9 +315,9 @@ def test_run_host_banded_pipeline(g, tile, cl):
     assert_close(Ch.numpy(), oracle.gemm(A, B))
 
 
-@pytest.mark.parametrize("tile,cl", SHAPES, ids=SHAPE_IDS)
+@pytest.mark.parametrize("tile,cl,mc", SHAPES, ids=SHAPE_IDS, indirect=["mc"])
 @pytest.mark.parametrize("mode", MODES)
-def test_grouped_varied_shapes_small(g, tile, cl, mode):
+def test_grouped_varied_shapes_small(g, tile, cl, mc, mode):
     """Problems of different M, N and K in one flat grid (ragged edges, an empty problem,
     a K = 0 problem whose C must be zero)."""
     shapes = [(300, 520, 192), (128, 256, 1000), (0, 256, 64), (700, 264, 64), (256, 776, 0), (64, 1024, 512)]
