@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--raster-group", type=int, default=8)
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="k-blocks prefetched into L2 (-1: library default)")
     ap.add_argument("--occupy", type=int, default=0, help="SMs held by an occupier kernel while timing")
-    ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent,clusters",
+    ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent,pdl,clusters",
                     help="comma-separated subset of the schedules to time (clc is always first)")
     return ap.parse_args()
 
@@ -320,17 +320,19 @@ def run_ours(args, ws, rank, local):
     wanted = set(args.modes.split(",")) | {"clc"}
     # "static_148" selects the planned static worker count of the workload's statement
     # (148 workers, or 74 pairs)
-    # (key, schedule, static workers, cluster size, B multicast for clusters of 2, selector)
-    table = [("clc", "clc", 0, cl, 0, "clc"),
-             (f"static_{planned}", "static", planned, cl, 0, "static_148"),
-             ("static_sms", "static", sms // cl, cl, 0, "static_sms"),
-             ("nonpersistent", "nonpersistent", 0, cl, 0, "nonpersistent")]
+    # (key, schedule, static workers, cluster size, B multicast for clusters of 2,
+    #  programmatic dependent launch, selector)
+    table = [("clc", "clc", 0, cl, 0, 0, "clc"),
+             (f"static_{planned}", "static", planned, cl, 0, 0, "static_148"),
+             ("static_sms", "static", sms // cl, cl, 0, 0, "static_sms"),
+             ("nonpersistent", "nonpersistent", 0, cl, 0, 0, "nonpersistent"),
+             ("clc_pdl", "clc", 0, cl, 0, 1, "pdl")]
     if cl == 1 and w.bn == 256:
         # the same tile on larger clusters: beside the headline, not part of it
-        table += [("clc_pair_256x256", "clc", 0, 2, 0, "clusters"),
-                  ("clc_cluster2_shared_b", "clc", 0, 2, 1, "clusters"),
-                  ("clc_cluster4_shared_b", "clc", 0, 4, 0, "clusters")]
-    order = [(k, m, n, c, mc) for k, m, n, c, mc, sel in table if sel in wanted]
+        table += [("clc_pair_256x256", "clc", 0, 2, 0, 0, "clusters"),
+                  ("clc_cluster2_shared_b", "clc", 0, 2, 1, 0, "clusters"),
+                  ("clc_cluster4_shared_b", "clc", 0, 4, 0, 0, "clusters")]
+    order = [(k, m, n, c, mc, pd) for k, m, n, c, mc, pd, sel in table if sel in wanted]
     step("clc")()                     # sizes the handle's workspace before any occupier runs
     torch.cuda.synchronize()
     if args.occupy:
@@ -343,8 +345,8 @@ def run_ours(args, ws, rank, local):
     launches = 0
     kernel_ms = None
     try:
-        for key, mode, nw, ccl, mcast in order:
-            g.set_opts(cluster_b_multicast=mcast)
+        for key, mode, nw, ccl, mcast, pdl in order:
+            g.set_opts(cluster_b_multicast=mcast, pdl=pdl)
             sampler = ClockSampler(local) if key == "clc" else None
             if sampler:
                 sampler.start()
@@ -359,13 +361,13 @@ def run_ours(args, ws, rank, local):
                           "pct_hbm_roofline": 100.0 * w.min_bytes / (total_ms / args.steps * 1e-3) / 1e9
                           / peaks["hbm_gbs"],
                           "workers": nw if mode == "static" else None, "cluster": ccl,
-                          "b_multicast": bool(mcast or ccl == 4)}
+                          "b_multicast": bool(mcast or ccl == 4), "pdl": bool(pdl)}
             if key == "clc":
                 launches = args.steps
                 kernel_ms = statistics.mean(per)
     finally:
         occ_status = g.occupy_stop() if args.occupy else 0
-        g.set_opts(cluster_b_multicast=0)
+        g.set_opts(cluster_b_multicast=0, pdl=0)
     torch.cuda.synchronize()
     g.sync(stream)
 

@@ -64,6 +64,7 @@ struct Params {
   int inject_fail_after;         // CLC: stop after this many successful cancels (<0: off)
   int l2_prefetch;               // k-blocks the producer prefetches into L2 ahead of its loads (0: off)
   int hold_scheduler;            // test hook: the CLC scheduler issues and signals nothing
+  int pdl;                       // launched as a programmatic dependent of the previous kernel
 };
 
 // Cluster shapes:
@@ -362,6 +363,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if constexpr (CL > 1) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
+  if (p.pdl) {
+    // Programmatic dependent launch: the prologue above touched no global memory, so it may
+    // overlap the previous kernel; everything below waits until that kernel has completed
+    // and its writes are visible.  The next kernel may be scheduled from now on (it waits
+    // the same way before touching memory).
+    griddep_launch_dependents();
+    griddep_wait();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer

@@ -103,6 +103,10 @@ typedef struct {
     int     cluster_b_multicast; /* clusters of 2: 0 (default) = CTA-pair MMA; 1 = each CTA runs
                                   its own 128 x 256 MMA and the pair shares the B tile by TMA
                                   multicast (clusters of 4 always work this way) */
+    int     pdl;               /* 1: launch as a programmatic dependent of the previous kernel
+                                  on the stream: the CTAs' prologue (barrier setup, tensor-memory
+                                  allocation) may overlap that kernel's tail, and every access to
+                                  global memory waits until it has completed.  Default 0 */
 } gemm_opts_t;
 
 /* Description of the last launch, filled by gemm_last_launch(). */
