@@ -44,3 +44,34 @@ def test_response_wait_times_out_and_is_reported(cl, mc):
         g.sync()
         assert g.device_error() == (0, 0, 0)
         assert_close(C2.cpu().numpy(), oracle.gemm(A, B))
+
+
+def test_higher_priority_kernels_stop_fetching_but_keep_coverage():
+    """A cancel may fail because the hardware wants to schedule a higher-priority kernel
+    ("CUTLASS CLC dynamic persistent kernel", section "Cluster granularity and exit after
+    failure").  A CLC GEMM on a low-priority stream shares the GPU with a stream of small
+    kernels at higher priority; whatever the cancels return, every tile is computed exactly
+    once and the result is exact."""
+    import blackwell_clc_dynamic_gb300 as m
+    M, N, K = 128 * 152 * 4, 512, 2048
+    A = wl.make_matrix((M, K), 131, "int")
+    B = wl.make_matrix((K, N), 132, "int")
+    dA, dB = A.cuda(), B.cuda()
+    lo, hi = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)
+    x = torch.zeros(1 << 20, device="cuda")
+    with m.Gemm(0) as g:
+        C = torch.full((M, N), float("nan"), device="cuda")
+        g.run(dA, dB, C, stream=lo)          # sizes the workspace
+        torch.cuda.synchronize()
+        C.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.run(dA, dB, C, stream=lo)
+        with torch.cuda.stream(hi):
+            for _ in range(200):
+                x.add_(1.0)
+        torch.cuda.synchronize()
+        g.sync(lo)
+        ref = oracle.gemm(A, B)
+        assert np.array_equal(C.cpu().numpy().astype(np.float64), ref)
+        owner_lin, first = check_log(g, "clc", [M // 128], N // 256, 1)
+        assert float(x[0]) == 200.0
