@@ -320,19 +320,24 @@ def run_ours(args, ws, rank, local):
     wanted = set(args.modes.split(",")) | {"clc"}
     # "static_148" selects the planned static worker count of the workload's statement
     # (148 workers, or 74 pairs)
-    # (key, schedule, static workers, cluster size, B multicast for clusters of 2,
-    #  programmatic dependent launch, selector)
-    table = [("clc", "clc", 0, cl, 0, 0, "clc"),
-             (f"static_{planned}", "static", planned, cl, 0, 0, "static_148"),
-             ("static_sms", "static", sms // cl, cl, 0, 0, "static_sms"),
-             ("nonpersistent", "nonpersistent", 0, cl, 0, 0, "nonpersistent"),
-             ("clc_pdl", "clc", 0, cl, 0, 1, "pdl")]
+    # one row per timed mode: schedule, static workers, cluster size, B multicast for clusters
+    # of 2, programmatic dependent launch, ownership log; `sel` names it in --modes
+    def row(key, sched, sel, nw=0, ccl=None, mcast=0, pdl=0, log=1):
+        return dict(key=key, sched=sched, sel=sel, nw=nw, cl=cl if ccl is None else ccl, mcast=mcast, pdl=pdl,
+                    log=log)
+    table = [row("clc", "clc", "clc"),
+             row(f"static_{planned}", "static", "static_148", nw=planned),
+             row("static_sms", "static", "static_sms", nw=sms // cl),
+             row("nonpersistent", "nonpersistent", "nonpersistent"),
+             row("clc_pdl", "clc", "pdl", pdl=1),
+             row("clc_no_log", "clc", "pdl", log=0),
+             row("clc_pdl_no_log", "clc", "pdl", pdl=1, log=0)]
     if cl == 1 and w.bn == 256:
         # the same tile on larger clusters: beside the headline, not part of it
-        table += [("clc_pair_256x256", "clc", 0, 2, 0, 0, "clusters"),
-                  ("clc_cluster2_shared_b", "clc", 0, 2, 1, 0, "clusters"),
-                  ("clc_cluster4_shared_b", "clc", 0, 4, 0, 0, "clusters")]
-    order = [(k, m, n, c, mc, pd) for k, m, n, c, mc, pd, sel in table if sel in wanted]
+        table += [row("clc_pair_256x256", "clc", "clusters", ccl=2),
+                  row("clc_cluster2_shared_b", "clc", "clusters", ccl=2, mcast=1),
+                  row("clc_cluster4_shared_b", "clc", "clusters", ccl=4)]
+    order = [r for r in table if r["sel"] in wanted]
     step("clc")()                     # sizes the handle's workspace before any occupier runs
     torch.cuda.synchronize()
     if args.occupy:
@@ -345,8 +350,9 @@ def run_ours(args, ws, rank, local):
     launches = 0
     kernel_ms = None
     try:
-        for key, mode, nw, ccl, mcast, pdl in order:
-            g.set_opts(cluster_b_multicast=mcast, pdl=pdl)
+        for r in order:
+            key, mode, nw, ccl, mcast, pdl = r["key"], r["sched"], r["nw"], r["cl"], r["mcast"], r["pdl"]
+            g.set_opts(cluster_b_multicast=mcast, pdl=pdl, log_enable=r["log"])
             sampler = ClockSampler(local) if key == "clc" else None
             if sampler:
                 sampler.start()
@@ -361,13 +367,13 @@ def run_ours(args, ws, rank, local):
                           "pct_hbm_roofline": 100.0 * w.min_bytes / (total_ms / args.steps * 1e-3) / 1e9
                           / peaks["hbm_gbs"],
                           "workers": nw if mode == "static" else None, "cluster": ccl,
-                          "b_multicast": bool(mcast or ccl == 4), "pdl": bool(pdl)}
+                          "b_multicast": bool(mcast or ccl == 4), "pdl": bool(pdl), "log": bool(r["log"])}
             if key == "clc":
                 launches = args.steps
                 kernel_ms = statistics.mean(per)
     finally:
         occ_status = g.occupy_stop() if args.occupy else 0
-        g.set_opts(cluster_b_multicast=0, pdl=0)
+        g.set_opts(cluster_b_multicast=0, pdl=0, log_enable=1)
     torch.cuda.synchronize()
     g.sync(stream)
 
@@ -549,6 +555,35 @@ def run_extras(g, args, peaks, sms):
         out["tail"].append(row)
         del dA, dB, C
         torch.cuda.empty_cache()
+
+    # higher-priority kernels competing with a CLC GEMM: cancels may fail early (the pages'
+    # second failure cause); count the workers that ran
+    w = wl.tail(296 * 4)
+    A, B = wl.make_inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    del A, B
+    lo, hi = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)
+    x = torch.zeros(1 << 20, device="cuda")
+    g.run(dA, dB, C, stream=lo)
+    torch.cuda.synchronize()
+    prio = {"workload": w.name, "tiles": w.M // 128}
+    for label, burst in (("alone", 0), ("with_200_high_priority_kernels", 200)):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(lo)
+        g.run(dA, dB, C, stream=lo)
+        ev1.record(lo)
+        with torch.cuda.stream(hi):
+            for _ in range(burst):
+                x.add_(1.0)
+        torch.cuda.synchronize()
+        owner, claims, first = g.get_log()
+        prio[label] = {"ms": ev0.elapsed_time(ev1), "workers_ran": int((first >= 0).sum()),
+                       "max_tiles_per_worker": int(np.bincount(owner).max()),
+                       "claims_exactly_once": bool((claims == 1).all())}
+    out["priority"] = prio
+    del dA, dB, C
+    torch.cuda.empty_cache()
 
     # CTA pairs while 24 SMs are held by an occupier on another stream
     w = wl.PAIR
