@@ -49,16 +49,16 @@ def test_response_wait_times_out_and_is_reported(cl, mc):
 def test_higher_priority_kernels_stop_fetching_but_keep_coverage():
     """A cancel may fail because the hardware wants to schedule a higher-priority kernel
     ("CUTLASS CLC dynamic persistent kernel", section "Cluster granularity and exit after
-    failure").  A CLC GEMM on a low-priority stream shares the GPU with a stream of small
-    kernels at higher priority; whatever the cancels return, every tile is computed exactly
-    once and the result is exact."""
+    failure").  A CLC GEMM runs on a low-priority stream; right after it, an occupier that
+    cannot share an SM with it (large shared-memory footprint) is launched on a
+    higher-priority stream.  Workers whose cancel fails stop and give their SM up; the
+    launches nobody took run later.  Every tile is still computed exactly once."""
     import blackwell_clc_dynamic_gb300 as m
-    M, N, K = 128 * 152 * 4, 512, 2048
+    M, N, K = 128 * 152 * 8, 256, 4096
     A = wl.make_matrix((M, K), 131, "int")
     B = wl.make_matrix((K, N), 132, "int")
     dA, dB = A.cuda(), B.cuda()
     lo, hi = torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-1)
-    x = torch.zeros(1 << 20, device="cuda")
     with m.Gemm(0) as g:
         C = torch.full((M, N), float("nan"), device="cuda")
         g.run(dA, dB, C, stream=lo)          # sizes the workspace
@@ -66,12 +66,14 @@ def test_higher_priority_kernels_stop_fetching_but_keep_coverage():
         C.fill_(float("nan"))
         torch.cuda.synchronize()
         g.run(dA, dB, C, stream=lo)
-        with torch.cuda.stream(hi):
-            for _ in range(200):
-                x.add_(1.0)
+        g.occupy_start(24, limit_ns=20_000_000_000, stream=hi)
+        try:
+            lo.synchronize()
+        finally:
+            timed_out = g.occupy_stop()
         torch.cuda.synchronize()
+        assert timed_out == 0
         g.sync(lo)
         ref = oracle.gemm(A, B)
         assert np.array_equal(C.cpu().numpy().astype(np.float64), ref)
         owner_lin, first = check_log(g, "clc", [M // 128], N // 256, 1)
-        assert float(x[0]) == 200.0
