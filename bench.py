@@ -524,6 +524,10 @@ def trace_stats(g, run_once):
     last = np.array([b - t0 for a, b in span.values()], dtype=np.float64)
     wait = tr[:, 4][tr[:, 4] > 0].astype(np.float64)
     rt = tr[:, 5][tr[:, 5] > 0].astype(np.float64)
+    epi_ok = ok & (tr[:, 6] > 0)
+    epilogue = (end[epi_ok] - tr[epi_ok, 6]).astype(np.float64)
+    main_ok = ok & (tr[:, 7] > 0)
+    mainloop = (tr[main_ok, 7] - start[main_ok]).astype(np.float64)
 
     def q(x):
         if x.size == 0:
@@ -535,7 +539,8 @@ def trace_stats(g, run_once):
                                   "max": float(busy.max() / 1e3)},
             "sm_last_end_us": {"min": float(last.min() / 1e3), "max": float(last.max() / 1e3)},
             "tile_us": q((end[ok] - start[ok]).astype(np.float64)),
-            "producer_wait_for_clc_response": q(wait), "try_cancel_round_trip": q(rt)}
+            "producer_wait_for_clc_response": q(wait), "try_cancel_round_trip": q(rt),
+            "epilogue_us": q(epilogue), "start_to_last_mma_us": q(mainloop)}
 
 
 def run_extras(g, args, peaks, sms):

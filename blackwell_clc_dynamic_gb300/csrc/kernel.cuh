@@ -58,7 +58,8 @@ struct Params {
   int* log_claims;               // [CTA tiles] times the tile was computed
   int* log_first;                // [launched workers] linear id of the worker's first tile
   unsigned long long* trace;     // [CTA tiles][8]: start ns, end ns, smid, worker, producer's wait
-                                 // for this tile's CLC response (ns), try_cancel round trip (ns)
+                                 // for this tile's CLC response (ns), try_cancel round trip (ns),
+                                 // epilogue start ns, last MMA issued ns
   int* err;                      // device error word
   long long timeout_ns;          // bound on every wait
   int inject_fail_after;         // CLC: stop after this many successful cancels (<0: off)
@@ -470,6 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (!ok) break;
         if constexpr (PAIR) mma_commit_pair(bar(C::BAR_ACC_FULL + acc), 0x3);
         else mma_commit(bar(C::BAR_ACC_FULL + acc));
+        if (p.trace) p.trace[TRACE_WORDS * (size_t)w.pos + 7] = globaltimer();
         acc ^= 1;
         if (acc == 0) aph ^= 1;
         w = it.next(p, rank, sb, ctl, false);
@@ -544,6 +546,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     while (w.valid) {
       if (!bar_wait(bar(C::BAR_ACC_FULL + acc), aph, p, ctl, WAIT_ACC_FULL)) break;
       tc_fence_after();
+      if (p.trace && q == 0 && lane == 0) p.trace[TRACE_WORDS * (size_t)w.pos + 6] = globaltimer();
       const CUtensorMap* mC = p.G ? p.gmaps + 3 * w.g + 2 : &p.tmC;
       const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1

@@ -217,7 +217,9 @@ CLCGEMM_API int gemm_get_log(gemm_handle_t h, int32_t *owner, int32_t *claims, i
  *   epilogue issued the tile's last store)  [2] SM id  [3] worker  [4] ns the producer
  *   waited for the CLC response that named this tile (0 for a worker's first tile and
  *   for the other schedules)  [5] ns from the try_cancel that returned this tile to the
- *   scheduler seeing its response (CLC, rank-0 tile only)  [6], [7] zero. */
+ *   scheduler seeing its response (CLC, rank-0 tile only)  [6] ns when the epilogue saw
+ *   the finished accumulator  [7] ns when the MMA warp issued the tile's last MMA
+ *   (rank 0 for CTA pairs). */
 CLCGEMM_API int gemm_get_trace(gemm_handle_t h, uint64_t *out, int64_t n_tiles);
 
 /* ---------------------------------------------------------------- occupancy */
