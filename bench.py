@@ -13,7 +13,7 @@ With N > 1 (torchrun, one rank per GPU) every rank runs an independent replica (
 path has no exchange step): weak scaling, max time over ranks.
 `--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
 `--all` also runs the tail sweep, the CTA-pair run beside an SM occupier and the
-grouped problem, and writes them to gpurun_out/bench_all.json.
+grouped problems, and writes them to a JSON file (--all-out, default bench_all.json).
 """
 from __future__ import annotations
 
@@ -53,7 +53,7 @@ def parse():
                     help="untimed back-to-back launches before the first timed mode, so every mode is timed "
                          "at the same power and clock state")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
-    ap.add_argument("--all-out", default=None, help="where --all writes its JSON (default gpurun_out/bench_all.json)")
+    ap.add_argument("--all-out", default="bench_all.json", help="where --all writes its JSON")
     ap.add_argument("--all-steps", type=int, default=60)
     ap.add_argument("--workload", default="square", help="square | pair | grouped | grouped_vk | tail<T> | tiny")
     ap.add_argument("--raster-group", type=int, default=8)
@@ -698,8 +698,7 @@ def run_extras(g, args, peaks, sms):
     out["grouped_varied_depth"] = vk
     g.sync(st)
 
-    path = args.all_out or (os.path.join(ROOT, "gpurun_out", "bench_all.json")
-                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "bench_all.json")
+    path = args.all_out
     with open(path, "w") as f:
         json.dump(out, f, indent=1)
     print(f"# --all results written to {path}", file=sys.stderr)
