@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           } else {
             // every CTA of the cluster receives the response at the same offset
 #pragma unroll
-            for (uint32_t r = 1; r < (uint32_t)CL; ++r) mbar_arrive_expect_tx_cluster(map_to_rank(full, r), 16);
+            for (uint32_t rk = 1; rk < (uint32_t)CL; ++rk) mbar_arrive_expect_tx_cluster(map_to_rank(full, rk), 16);
             clc_try_cancel_all(resp, full);
           }
         } else {
@@ -509,10 +509,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           misc[2 + s] = 1;
           mbar_arrive(full);
 #pragma unroll
-          for (uint32_t r = 1; r < (uint32_t)CL; ++r) {
-            const uint32_t peer_flag = map_to_rank(smem_addr((const void*)(misc + 2 + s)), r);
+          for (uint32_t rk = 1; rk < (uint32_t)CL; ++rk) {
+            const uint32_t peer_flag = map_to_rank(smem_addr((const void*)(misc + 2 + s)), rk);
             asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_flag), "r"(1u) : "memory");
-            mbar_arrive_cluster(map_to_rank(full, r));
+            mbar_arrive_cluster(map_to_rank(full, rk));
           }
         }
         // the scheduler consumes the response too: it stops at the first failure
