@@ -353,3 +353,23 @@ def test_grouped_varied_depth_full_size_sampled(g, mode):
         _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
                        blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
     check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("dT", ["1", "sms-1", "sms", "sms+1", "2sms+1"])
+@pytest.mark.parametrize("mode", ["clc", "static"])
+def test_tile_count_around_the_sm_count(g, dT, mode):
+    """Fewer, as many and slightly more tiles than resident workers, relative to the queried
+    SM count: coverage stays exact and static workers follow t mod W."""
+    sms = g.sm_count
+    T = {"1": 1, "sms-1": sms - 1, "sms": sms, "sms+1": sms + 1, "2sms+1": 2 * sms + 1}[dT]
+    M, N, K = 128 * T, 256, 512
+    A = wl.make_matrix((M, K), 141, "int")
+    B = wl.make_matrix((K, N), 142, "int")
+    C = run(g, A, B, sched=mode, num_workers=sms)
+    assert np.array_equal(C.astype(np.float64), oracle.gemm(A, B))
+    owner_lin, first = check_log(g, mode, [T], 1, 1, num_workers=sms if mode == "static" else None)
+    if mode == "static":
+        assert owner_lin == cv.expected_owner_static(T, sms)
+    else:
+        # at most one worker per resident slot plus the launches nobody took
+        assert len(set(owner_lin)) <= T
