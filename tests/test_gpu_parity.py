@@ -373,3 +373,25 @@ def test_tile_count_around_the_sm_count(g, dT, mode):
     else:
         # at most one worker per resident slot plus the launches nobody took
         assert len(set(owner_lin)) <= T
+
+
+def test_randomized_shapes_and_modes(g):
+    """24 seeded random problems: ragged M, N, K (multiples of 8 where the ABI needs it),
+    every schedule and cluster shape, integer inputs so the result must be bit-exact."""
+    rng = np.random.default_rng(2024)
+    configs = [(TILE_256, 1, 0), (TILE_128, 1, 0), (TILE_256, 2, 0), (TILE_256, 2, 1), (TILE_256, 4, 0)]
+    try:
+        for i in range(24):
+            tile, cl, mcast = configs[i % len(configs)]
+            mode = MODES[(i // len(configs)) % 3]
+            M = int(rng.integers(1, 1500))
+            N = 8 * int(rng.integers(1, 160))
+            K = 8 * int(rng.integers(0, 200))
+            A = wl.make_matrix((M, K), 1000 + i, "int")
+            B = wl.make_matrix((K, N), 2000 + i, "int")
+            g.set_opts(cluster_b_multicast=mcast, raster_group=int(rng.integers(1, 17)))
+            C = run(g, A, B, tile=tile, cluster=cl, sched=mode, num_workers=int(rng.integers(1, 300)))
+            ref = oracle.gemm(A, B) if K else np.zeros((M, N))
+            assert np.array_equal(C.astype(np.float64), ref), (i, M, N, K, tile, cl, mcast, mode)
+    finally:
+        g.set_opts(cluster_b_multicast=0, raster_group=8)
