@@ -493,6 +493,24 @@ def time_stream(fn, steps, warmup, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_stream_flushed(fn, steps, warmup, stream, flush):
+    """Like time_stream, but L2 is flushed (a buffer larger than L2 is overwritten) before
+    every timed launch; the flush lies outside the timed events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        with torch.cuda.stream(stream):
+            flush.add_(1)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def summarise(per_ms, flops, min_bytes, peaks):
     med = statistics.median(per_ms)
     mean = statistics.mean(per_ms)
@@ -553,8 +571,10 @@ def run_extras(g, args, peaks, sms):
     steps, warm = args.all_steps, 5
     st = torch.cuda.Stream()
 
-    # tail sweep: M = 128 T, N = 256, K = 8192 (seed 2): CLC vs static
+    # tail sweep: M = 128 T, N = 256, K = 8192 (seed 2): CLC vs static, with and without an
+    # L2 flush (256 MiB write) before every timed launch
     resident = g.max_active_clusters((128, 256, 64), 1)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
     for T in wl.TAIL_T:
         w = wl.tail(T)
         A, B = wl.make_inputs(w)
@@ -566,11 +586,15 @@ def run_extras(g, args, peaks, sms):
         for key, mode, nw in (("clc", "clc", 0), ("static_148", "static", 148), ("static_sms", "static", sms)):
             per = time_stream(lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st), steps, warm, st)
             row[key] = summarise(per, w.flops, w.min_bytes, peaks)
+            per = time_stream_flushed(lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st), steps, warm,
+                                      st, flush)
+            row[key]["l2_flushed"] = summarise(per, w.flops, w.min_bytes, peaks)
             if T in (149, 297) and key != "static_sms":
                 row[key]["trace"] = trace_stats(g, lambda: g.run(dA, dB, C, sched=mode, num_workers=nw, stream=st))
         out["tail"].append(row)
         del dA, dB, C
         torch.cuda.empty_cache()
+    del flush
 
     # a higher-priority kernel that cannot share an SM with the GEMM arrives while a CLC
     # GEMM runs: cancels may fail early (the pages' second failure cause); count the
