@@ -395,3 +395,21 @@ def test_randomized_shapes_and_modes(g):
             assert np.array_equal(C.astype(np.float64), ref), (i, M, N, K, tile, cl, mcast, mode)
     finally:
         g.set_opts(cluster_b_multicast=0, raster_group=8)
+
+
+@pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0)], ids=["pair", "c2_shared_b", "c4_shared_b"])
+def test_square_full_size_cluster_modes(g, cl, mcast):
+    """The square workload in the cluster launch configurations the benchmark times beside
+    the headline (CLC): sampled elements and whole tiles against the oracle, exact log."""
+    w = wl.SQUARE
+    A, B = _inputs(w)
+    g.set_opts(cluster_b_multicast=mcast)
+    try:
+        C = torch.full((w.M, w.N), float("nan"), device="cuda")
+        g.run(A.cuda(), B.cuda(), C, cluster=cl, sched="clc")
+        g.sync()
+        _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(20 + cl + mcast),
+                       blocks=[(0, 128 * cl, 0, 256), (w.M - 128 * cl, w.M, w.N - 256, w.N)])
+        check_log(g, "clc", [w.M // (128 * cl)], w.N // 256, cl)
+    finally:
+        g.set_opts(cluster_b_multicast=0)
