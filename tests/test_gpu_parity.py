@@ -413,3 +413,38 @@ def test_square_full_size_cluster_modes(g, cl, mcast):
         check_log(g, "clc", [w.M // (128 * cl)], w.N // 256, cl)
     finally:
         g.set_opts(cluster_b_multicast=0)
+
+
+@pytest.mark.parametrize("cl,mcast,mode", [(1, 0, "clc"), (1, 0, "static"), (2, 0, "clc"), (4, 0, "clc")],
+                         ids=["c1-clc", "c1-static", "pair-clc", "c4-clc"])
+def test_trace_is_consistent_with_the_log(g, cl, mcast, mode):
+    """Per tile: producer start <= last MMA issued <= epilogue start <= last store issued;
+    the SM id is below the SM count; the worker is the one the ownership log names; CLC
+    round trips are recorded only for tiles that came from a cancel."""
+    M, N, K = 128 * cl * 40, 512, 1024
+    A = wl.make_matrix((M, K), 151)
+    B = wl.make_matrix((K, N), 152)
+    g.set_opts(trace_enable=1, cluster_b_multicast=mcast)
+    try:
+        C = run(g, A, B, cluster=cl, sched=mode, num_workers=37)
+        tr = g.get_trace().astype(np.int64)
+        owner, claims, first = g.get_log()
+    finally:
+        g.set_opts(trace_enable=0, cluster_b_multicast=0)
+    assert_close(C, oracle.gemm(A, B))
+    start, end, sm, worker, wait, rt, epi, last_mma = (tr[:, i] for i in range(8))
+    assert np.all(start > 0) and np.all(end >= start) and np.all(epi >= start) and np.all(end >= epi)
+    # CTA tiles are row-major over (M/128) x (N/256); the CTA of rank r holds row block
+    # cl*m + r.  The MMA time is recorded by the CTA that issues the MMA: every CTA, or
+    # rank 0 of a CTA pair.
+    rank = (np.arange(len(tr)) // (N // 256)) % cl
+    issuer = np.ones(len(tr), dtype=bool) if (cl == 1 or mcast or cl == 4) else rank == 0
+    assert np.all(last_mma[issuer] >= start[issuer]) and np.all(epi[issuer] >= last_mma[issuer])
+    assert np.all(sm < g.sm_count)
+    assert np.array_equal(worker, owner.astype(np.int64))
+    if mode == "static":
+        assert np.all(rt == 0)
+    else:
+        # round trips are written by the scheduler of rank 0 for the tiles its cancels
+        # returned; a worker's own first tile has none
+        assert np.all(rt[rank != 0] == 0)
