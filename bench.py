@@ -402,6 +402,18 @@ def run_ours(args, ws, rank, local):
                "h2d_bytes_per_step": A.numel() * 2 + B.numel() * 2, "d2h_bytes_per_step": Ch.numel() * 4,
                "steps": n_e2e, "ms_per_step": tot / n_e2e, "api": "gemm_run_host (pinned host buffers)"}
 
+    # one traced launch per schedule (outside the timed region): how evenly the SMs finish
+    # and what consuming CLC responses costs
+    traced = {}
+    if not args.occupy:
+        for key, mode, nw in (("clc", "clc", 0), (f"static_{planned}", "static", planned)):
+            st = trace_stats(g, step(mode, nw))
+            traced[key] = {"launch_span_us": round(st["kernel_span_us"], 1),
+                           "sm_last_end_spread_us": round(st["sm_last_end_us"]["max"] - st["sm_last_end_us"]["min"], 1),
+                           "producer_wait_for_clc_response_us": st["producer_wait_for_clc_response"],
+                           "try_cancel_round_trip_us": st["try_cancel_round_trip"],
+                           "epilogue_us_mean": st["epilogue_us"]["mean_us"] if st["epilogue_us"] else None}
+
     if rank != 0:
         g.close()
         if ws > 1:
@@ -438,7 +450,7 @@ def run_ours(args, ws, rank, local):
         "pct_of_bf16_peak_burst": clc_m["pct_bf16_peak_burst"],
         "pct_of_bf16_peak_sustained": clc_m["pct_bf16_peak_sustained"],
         "modes": modes, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches, "clocks": clocks,
+        "gpu_launches": launches, "clocks": clocks, "traced_launch": traced,
     }
     if args.occupy:
         line["occupier_hit_time_limit"] = bool(occ_status)
