@@ -427,7 +427,8 @@ def run_ours(args, ws, rank, local):
     clc_m = modes["clc"]
     achieved = w.flops / (kernel_ms * 1e-3) / 1e12
     kname = f"gemm_kernel<{w.bn},{cl},CLC>"
-    traffic = traffic_for(f"gemm_n{w.bn}_c{cl}_clc_{args.workload}", args.raster_group, int(g.opts.l2_prefetch))
+    l2_pf = args.l2_prefetch if args.l2_prefetch >= 0 else 0   # the library's default distance is 0
+    traffic = traffic_for(f"gemm_n{w.bn}_c{cl}_clc_{args.workload}", args.raster_group, l2_pf)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
             "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": traffic,
             "peak_kind": f"bf16_tflops_sustained ({peaks_src}); timed region is a back-to-back loop",
@@ -442,7 +443,7 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded bf16, see workloads.py)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "tile": list(tile),
                    "cluster": [cl, 1, 1], "sched": "clc", "parallelism": f"replicas x{ws}",
-                   "raster_group": args.raster_group, "l2_prefetch": int(g.opts.l2_prefetch),
+                   "raster_group": args.raster_group, "l2_prefetch": l2_pf,
                    "occupied_sms": args.occupy,
                    "l2": ("no flush: operands and C exceed the 129 MB L2" if big
                           else "no flush (small case; parity only)"),
