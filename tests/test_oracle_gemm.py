@@ -130,3 +130,28 @@ def test_planted_transpose_is_caught():
     wrong = oracle.gemm(a.to(torch.bfloat16), b.t().contiguous().to(torch.bfloat16))
     ref = a.numpy().astype(np.int64) @ b.numpy().astype(np.int64)
     assert not np.array_equal(wrong, ref.astype(np.float64))
+
+
+def test_entries_against_exact_rationals():
+    rng = np.random.default_rng(11)
+    M, N, K = 9, 13, 11
+    A = _rand_bits(rng, (M, K), -2, 2)
+    B = _rand_bits(rng, (K, N), -2, 2)
+    rows = rng.integers(0, M, 30)
+    cols = rng.integers(0, N, 30)
+    got = oracle.gemm_entries(A, B, rows, cols)
+    u = Fraction(1, 2 ** 53)
+    gamma = (K - 1) * u / (1 - (K - 1) * u)
+    for e, (i, j) in enumerate(zip(rows, cols)):
+        terms = [ieee_bf16_value(int(A[i, k])) * ieee_bf16_value(int(B[k, j])) for k in range(K)]
+        assert abs(Fraction(got[e]) - sum(terms, Fraction(0))) <= gamma * sum(abs(t) for t in terms)
+
+
+def test_block_against_numpy_int64():
+    import torch
+    g = torch.Generator().manual_seed(12)
+    a = torch.randint(-4, 5, (70, 300), generator=g)
+    b = torch.randint(-4, 5, (300, 90), generator=g)
+    blk = oracle.gemm_block(a.to(torch.bfloat16), b.to(torch.bfloat16), 17, 61, 5, 83)
+    ref = a.numpy().astype(np.int64)[17:61] @ b.numpy().astype(np.int64)[:, 5:83]
+    assert np.array_equal(blk, ref.astype(np.float64))
