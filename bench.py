@@ -732,6 +732,15 @@ def run_extras(g, args, peaks, sms):
         if key in ("clc", "static_148"):
             vk[key]["trace"] = trace_stats(g, lambda: g.run_grouped_v(dA, dB, dC, sched=mode, num_workers=nw,
                                                                       stream=st))
+    # how far ahead a worker may fetch (the throttle): extra tiles held in reserve
+    vk["fetch_ahead"] = {}
+    for ahead in (0, 1, 2):
+        g.set_opts(fetch_ahead=ahead)
+        per = time_stream(lambda: g.run_grouped_v(dA, dB, dC, sched="clc", stream=st), steps, warm, st)
+        vk["fetch_ahead"][str(ahead)] = summarise(per, w.flops, w.min_bytes, peaks)
+        vk["fetch_ahead"][str(ahead)]["trace"] = trace_stats(
+            g, lambda: g.run_grouped_v(dA, dB, dC, sched="clc", stream=st))
+    g.set_opts(fetch_ahead=0)
     out["grouped_varied_depth"] = vk
     g.sync(st)
 

@@ -54,7 +54,8 @@ class gemm_cluster_t(ctypes.Structure):
 class gemm_opts_t(ctypes.Structure):
     _fields_ = [("log_enable", ctypes.c_int), ("trace_enable", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
                 ("inject_fail_after", ctypes.c_int), ("raster_group", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
-                ("hold_scheduler", ctypes.c_int), ("cluster_b_multicast", ctypes.c_int), ("pdl", ctypes.c_int)]
+                ("hold_scheduler", ctypes.c_int), ("cluster_b_multicast", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("fetch_ahead", ctypes.c_int)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
@@ -237,9 +238,11 @@ class Gemm:
 
     def __init__(self, device: int = 0, log: bool = True, trace: bool = False, timeout_ns: int = 0,
                  inject_fail_after: int = -1, raster_group: int = 8, l2_prefetch: int = -1,
-                 hold_scheduler: bool = False, cluster_b_multicast: bool = False, pdl: bool = False):
+                 hold_scheduler: bool = False, cluster_b_multicast: bool = False, pdl: bool = False,
+                 fetch_ahead: int = 0):
         self.opts = gemm_opts_t(int(log), int(trace), int(timeout_ns), int(inject_fail_after), int(raster_group),
-                                int(l2_prefetch), int(hold_scheduler), int(cluster_b_multicast), int(pdl))
+                                int(l2_prefetch), int(hold_scheduler), int(cluster_b_multicast), int(pdl),
+                                int(fetch_ahead))
         rc, h = gemm_create(device, self.opts)
         _check(rc, "gemm_create")
         self.h = h

@@ -66,6 +66,7 @@ struct Params {
   int l2_prefetch;               // k-blocks the producer prefetches into L2 ahead of its loads (0: off)
   int hold_scheduler;            // test hook: the CLC scheduler issues and signals nothing
   int pdl;                       // launched as a programmatic dependent of the previous kernel
+  int fetch_ahead;               // extra throttle tokens: the scheduler fetches this many more tiles ahead
 };
 
 // Cluster shapes:
@@ -383,12 +384,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       int tile = 0;
       const uint32_t full0_leader = PAIR ? map_to_rank(bar(C::BAR_FULL), 0) : bar(C::BAR_FULL);
       constexpr uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
-      while (w.valid) {
+      // throttle: one token per tile started; the scheduler issues fetch r only after token
+      // r, so it fetches tile r + 1 once tile r - fetch_ahead has started (default: once tile
+      // r has started, one tile ahead)
+      auto produce_token = [&](int tok) -> bool {
+        const int t = tok % THR_DEPTH;
+        if (!bar_wait(bar(C::BAR_THR_EMPTY + t), ((tok / THR_DEPTH) & 1) ^ 1, p, ctl, WAIT_THR_EMPTY)) return false;
+        mbar_arrive(bar(C::BAR_THR_FULL + t));
+        return true;
+      };
+      const int ahead = (SCHED == SCHED_CLC && rank == 0) ? min(max(p.fetch_ahead, 0), THR_DEPTH - 1) : 0;
+      bool tok_ok = true;
+      for (int tok = 0; tok < ahead && w.valid && tok_ok; ++tok) tok_ok = produce_token(tok);
+      while (w.valid && tok_ok) {
         if (SCHED == SCHED_CLC && rank == 0) {
-          // throttle: one token per tile started; the scheduler fetches only after it
-          const int t = tile % THR_DEPTH;
-          if (!bar_wait(bar(C::BAR_THR_EMPTY + t), ((tile / THR_DEPTH) & 1) ^ 1, p, ctl, WAIT_THR_EMPTY)) break;
-          mbar_arrive(bar(C::BAR_THR_FULL + t));
+          if (!produce_token(tile + ahead)) break;
         }
         if (p.trace) p.trace[TRACE_WORDS * (size_t)w.pos + 0] = globaltimer();
         const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;

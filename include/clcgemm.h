@@ -107,6 +107,10 @@ typedef struct {
                                   on the stream: the CTAs' prologue (barrier setup, tensor-memory
                                   allocation) may overlap that kernel's tail, and every access to
                                   global memory waits until it has completed.  Default 0 */
+    int     fetch_ahead;       /* CLC throttle: 0 (default) = a worker fetches its next tile once
+                                  its current tile has started (one tile ahead); 1 or 2 = that many
+                                  tiles further ahead (held in reserve, which can unbalance the
+                                  tail when tiles differ in cost).  Clamped to [0, 2] */
 } gemm_opts_t;
 
 /* Description of the last launch, filled by gemm_last_launch(). */

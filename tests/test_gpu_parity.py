@@ -448,3 +448,20 @@ def test_trace_is_consistent_with_the_log(g, cl, mcast, mode):
         # round trips are written by the scheduler of rank 0 for the tiles its cancels
         # returned; a worker's own first tile has none
         assert np.all(rt[rank != 0] == 0)
+
+
+@pytest.mark.parametrize("ahead", [1, 2])
+@pytest.mark.parametrize("cl", [1, 2])
+def test_fetch_ahead_keeps_coverage(g, ahead, cl):
+    """With extra throttle tokens a worker holds up to 1 + ahead fetched tiles; results and
+    coverage do not change."""
+    M, N, K = 128 * cl * 50, 512, 512
+    A = wl.make_matrix((M, K), 181, "int")
+    B = wl.make_matrix((K, N), 182, "int")
+    g.set_opts(fetch_ahead=ahead)
+    try:
+        C = run(g, A, B, cluster=cl, sched="clc")
+    finally:
+        g.set_opts(fetch_ahead=0)
+    assert np.array_equal(C.astype(np.float64), oracle.gemm(A, B))
+    check_log(g, "clc", [50], 2, cl)
