@@ -54,9 +54,12 @@ struct Params {
   int total;                     // cluster tiles in the launch
   int k_blocks;                  // ceil(K / BK)
   int raster_group;              // tile rows per raster band
-  int* log_owner;                // [CTA tiles] worker that computed the tile (or null)
-  int* log_claims;               // [CTA tiles] times the tile was computed
-  int* log_first;                // [launched workers] linear id of the worker's first tile
+  // Ownership log.  Entries carry the tag of the launch that wrote them, so a launch needs
+  // no clearing pass: an entry with another launch's tag reads as "not written".
+  int* log_owner;                // [CTA tiles] worker that computed the tile (or null: no log)
+  unsigned* log_claims;          // [CTA tiles] (tag << 8) | times the tile was computed (saturates at 255)
+  unsigned long long* log_first; // [launched workers] (tag << 32) | linear id of the worker's first tile
+  unsigned log_epoch;            // this launch's tag, in [1, 2^24)
   unsigned long long* trace;     // [CTA tiles][8]: start ns, end ns, smid, worker, producer's wait
                                  // for this tile's CLC response (ns), try_cancel round trip (ns),
                                  // epilogue start ns, last MMA issued ns
@@ -229,6 +232,21 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
   w.pos = base * CL + w.m_blk * nt + n;
   w.kb = kb;
   return w;
+}
+
+// ---------------------------------------------------------------- ownership log
+// Count one more computation of a tile in this launch.  A claim word written by another
+// launch (another tag) restarts at 1.  Each failed compare-and-swap means another claimant
+// of the same tile succeeded, so the loop ends after at most as many rounds as there are
+// claimants; the bound only guards a word that something else keeps rewriting.
+__device__ __forceinline__ void log_claim(unsigned* word, unsigned epoch) {
+  unsigned old = *reinterpret_cast<volatile unsigned*>(word);
+  for (int i = 0; i < 1024; ++i) {
+    const unsigned cnt = (old >> 8) == epoch ? min((old & 0xFFu) + 1u, 0xFFu) : 1u;
+    const unsigned prev = atomicCAS(word, old, (epoch << 8) | cnt);
+    if (prev == old) return;
+    old = prev;
+  }
 }
 
 // ---------------------------------------------------------------- bounded waits
@@ -604,8 +622,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       if (q == 0 && lane == 0) {
         if (p.log_owner) {
           p.log_owner[w.pos] = worker;
-          atomicAdd(p.log_claims + w.pos, 1);
-          if (first_tile && rank == 0) p.log_first[worker] = w.c;
+          log_claim(p.log_claims + w.pos, p.log_epoch);
+          if (first_tile && rank == 0)
+            p.log_first[worker] = ((unsigned long long)p.log_epoch << 32) | (unsigned)w.c;
         }
         if (p.trace) {
           p.trace[TRACE_WORDS * (size_t)w.pos + 1] = globaltimer();

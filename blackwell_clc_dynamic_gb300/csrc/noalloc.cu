@@ -13,9 +13,11 @@
 //     call; larger problems are rejected with GEMM_ERR_SCRATCH_LIMIT before anything is
 //     launched;
 //   - every call on a device uses the same array and leaves its contents behind; each
-//     call clears the parts that must start at zero (error word, claim counts) on its
-//     stream before its kernel.  Calls that overlap on the GPU (other streams, other
-//     threads) race on the array: serialise them.
+//     call clears the error word on its stream before its kernel and tags its log
+//     entries with a per-device launch counter (the array starts zeroed, tag 0 means
+//     unwritten, and the log part is cleared again only when the 24-bit tag wraps).
+//     Calls that overlap on the GPU (other streams, other threads) race on the array:
+//     serialise them.
 //   - the first call on a device (with that device current) looks up the array's
 //     device address with cudaGetSymbolAddress; make that first call before any stream
 //     capture begins.
@@ -38,15 +40,17 @@ namespace {
 constexpr int64_t kNoAllocMaxTiles = 65536;     // CTA tiles (ownership-log entries)
 constexpr int64_t kNoAllocMaxWorkers = 65536;   // launched workers (first-tile entries)
 constexpr int64_t kErrWords = 4;
-constexpr int64_t kScratchWords = kErrWords + 2 * kNoAllocMaxTiles + kNoAllocMaxWorkers;   // 768 KiB + 16 B
+constexpr int64_t kScratchWords = kErrWords + 2 * kNoAllocMaxTiles + 2 * kNoAllocMaxWorkers;   // 1 MiB + 16 B
 
-// [0, 4) error word | owner[kNoAllocMaxTiles] | claims[kNoAllocMaxTiles] | first[kNoAllocMaxWorkers]
+// [0, 4) error word | owner[kNoAllocMaxTiles] | claims[kNoAllocMaxTiles] |
+// first[kNoAllocMaxWorkers] (64-bit entries, 8-byte aligned)
 static __device__ __align__(256) int32_t g_noalloc_scratch[kScratchWords];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t* g_scratch_dev[kMaxDevices];   // device address of g_noalloc_scratch, per device
 int g_sms[kMaxDevices];
+uint32_t g_epoch[kMaxDevices];         // log tag of the device's most recent call
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int from_cuda(cudaError_t e) {
@@ -141,13 +145,21 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   int32_t* err = g_scratch_dev[dev];
   int32_t* owner = err + kErrWords;
-  int32_t* claims = owner + kNoAllocMaxTiles;
-  int32_t* first = claims + kNoAllocMaxTiles;
+  uint32_t* claims = reinterpret_cast<uint32_t*>(owner + kNoAllocMaxTiles);
+  unsigned long long* first = reinterpret_cast<unsigned long long*>(claims + kNoAllocMaxTiles);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t epoch;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    epoch = g_epoch[dev] + 1;
+    if (epoch >= (1u << 24)) epoch = 1;
+    g_epoch[dev] = epoch;
+  }
   e = cudaMemsetAsync(err, 0, kErrWords * sizeof(int32_t), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(owner, 0xFF, (size_t)n_tiles * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(claims, 0, (size_t)n_tiles * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(first, 0xFF, (size_t)workers * 4, s);
+  if (e == cudaSuccess && epoch == 1) {
+    e = cudaMemsetAsync(claims, 0, (size_t)kNoAllocMaxTiles * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(first, 0, (size_t)kNoAllocMaxWorkers * 8, s);
+  }
   if (e != cudaSuccess) return from_cuda(e);
 
   Params p;
@@ -173,6 +185,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   p.log_owner = owner;
   p.log_claims = claims;
   p.log_first = first;
+  p.log_epoch = epoch;
   p.trace = nullptr;
   p.err = err;
   p.timeout_ns = 2000000000LL;

@@ -206,12 +206,16 @@ CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
 
 /* gemm_get_log: copy-out of the most recent run's ownership log; waits for that run's
  * stream only (pageable `owner`/`claims`/`first` memory is fine).
- *   owner[n_tiles]     worker (cluster launch id) that computed each CTA tile
- *   claims[n_tiles]    how many times each CTA tile was computed (1 when correct)
+ *   owner[n_tiles]     worker (cluster launch id) that computed each CTA tile, -1 if
+ *                      no worker did
+ *   claims[n_tiles]    how many times each CTA tile was computed (1 when correct;
+ *                      counts saturate at 255)
  *   first[n_workers]   linear id of each worker's first tile, -1 if the worker never ran
  * CTA tiles are indexed row-major over (M / 128) x (N / bn) per problem, problems in
  * order.  Any output pointer may be NULL.  n_tiles / n_workers must equal the values
- * gemm_last_launch() reports. */
+ * gemm_last_launch() reports.  On the device every entry carries a tag of the launch
+ * that wrote it, so logging needs no clearing pass before a launch; this call keeps
+ * only the entries of the most recent launch. */
 CLCGEMM_API int gemm_get_log(gemm_handle_t h, int32_t *owner, int32_t *claims, int32_t *first,
                  int64_t n_tiles, int64_t n_workers);
 
@@ -255,7 +259,7 @@ CLCGEMM_API int gemm_occupy_stop(gemm_handle_t h, int *status);
  *   - No handle: it runs on the current device with the default options (ownership log
  *     on, 2 s wait bound, raster band 8).  Same arguments and shape rules as gemm_run.
  *   - Its scratch (device error word and ownership log) is one fixed file-scope device
- *     array of 768 KiB + 16 B, held by every GPU that loads the library until the process
+ *     array of 1 MiB + 16 B, held by every GPU that loads the library until the process
  *     exits.  At most 65536 CTA tiles and 65536 launched workers per call; larger
  *     problems return GEMM_ERR_SCRATCH_LIMIT and launch nothing.
  *   - It calls no cudaMalloc / cudaFree and no allocating library routine.

@@ -141,6 +141,35 @@ def test_static_owner_map_exact(g, T):
         assert owner_lin == cv.expected_owner_static(6 * T, W)
 
 
+def test_log_keeps_only_the_latest_launch():
+    """The device log is tagged per launch instead of cleared before it: entries of an
+    earlier, larger launch on the same handle must not show through a later, smaller one,
+    nor through a launch that ran with the log switched off."""
+    import blackwell_clc_dynamic_gb300 as m
+    h = m.Gemm(0)
+    try:
+        A = wl.make_matrix((128 * 8, 64), 71)
+        B = wl.make_matrix((64, 256 * 8), 72)
+        assert_close(run(h, A, B, sched="clc"), oracle.gemm(A, B))          # 64 tiles, 64 workers
+        check_log(h, "clc", [8], 8, 1)
+        a = wl.make_matrix((128 * 2, 64), 73)
+        b = wl.make_matrix((64, 256 * 4), 74)
+        assert_close(run(h, a, b, sched="static", num_workers=32), oracle.gemm(a, b))
+        check_log(h, "static", [2], 4, 1, num_workers=32)                  # workers 8..31 never ran
+        owner, claims, first = h.get_log()
+        assert claims.tolist() == [1] * 8 and first[8:].tolist() == [-1] * 24
+        h.set_opts(log_enable=0)
+        run(h, A, B, sched="clc")
+        h.set_opts(log_enable=1)
+        assert_close(run(h, a, b, sched="nonpersistent"), oracle.gemm(a, b))
+        check_log(h, "nonpersistent", [2], 4, 1)
+        assert_close(run(h, A, B, sched="clc"), oracle.gemm(A, B))
+        owner, claims, first = h.get_log()
+        assert claims.tolist() == [1] * 64 and sorted(set(owner.tolist())) == sorted(set(first.tolist()) - {-1})
+    finally:
+        h.close()
+
+
 @pytest.mark.parametrize("n_fetch", [0, 1, 5])
 def test_clc_injected_failure_keeps_coverage(g, n_fetch):
     """After n successful fetches the scheduler reports a failed fetch without issuing a
