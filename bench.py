@@ -339,7 +339,8 @@ def run_ours(args, ws, rank, local):
         # the same tile on larger clusters: beside the headline, not part of it
         table += [row("clc_pair_256x256", "clc", "clusters", ccl=2),
                   row("clc_cluster2_shared_b", "clc", "clusters", ccl=2, mcast=1),
-                  row("clc_cluster4_shared_b", "clc", "clusters", ccl=4)]
+                  row("clc_cluster4_shared_b", "clc", "clusters", ccl=4),
+                  row("clc_cluster2x2_shared_ab", "clc", "clusters", ccl=(2, 2, 1))]
     order = [r for r in table if r["sel"] in wanted]
     step("clc")()                     # sizes the handle's workspace before any occupier runs
     torch.cuda.synchronize()
@@ -378,7 +379,7 @@ def run_ours(args, ws, rank, local):
                           "pct_hbm_roofline": 100.0 * w.min_bytes / (total_ms / args.steps * 1e-3) / 1e9
                           / peaks["hbm_gbs"],
                           "workers": nw if mode == "static" else None, "cluster": ccl,
-                          "b_multicast": bool(mcast or ccl == 4), "pdl": bool(pdl), "log": bool(r["log"])}
+                          "b_multicast": bool(mcast or ccl in (4, (2, 2, 1))), "pdl": bool(pdl), "log": bool(r["log"])}
             if key == "clc":
                 launches = args.steps
                 kernel_ms = statistics.mean(per)

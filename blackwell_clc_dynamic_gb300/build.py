@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libclcgemm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "kern_n128_c1.cu", "kern_n256_c1.cu", "kern_n256_c2.cu", "kern_n256_c2mc.cu", "kern_n256_c4mc.cu",
+SOURCES = ["api.cu", "kern_n128_c1.cu", "kern_n256_c1.cu", "kern_n256_c2.cu", "kern_n256_c2mc.cu", "kern_n256_c4mc.cu", "kern_n256_c2x2.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -79,12 +79,24 @@ struct Params {
 //   CL == 2 or 4, !PAIR  CL CTAs each run their own 128 x BN MMA on consecutive row blocks
 //                      and share the B tile: each loads 1/CL of it and multicasts that part
 //                      to every CTA of the cluster
-template <int BN_, int CL_, bool PAIR_>
+//   CL == 4, RN == 2   a 2 x 2 cluster: each CTA runs its own 128 x BN MMA on one quarter of a
+//                      256 x 2BN cluster tile; the two CTAs of a row share their A tile (each
+//                      loads half of its rows), the two CTAs of a column share their B tile
+//                      (each loads half of its boxes), both by multicast
+// RN is the number of CTAs of a cluster along N; RM = CL / RN along M.  Cluster rank r sits
+// at row r / RN, column r % RN of the cluster tile.  Clusters with RN == 1 are launched as
+// CL x 1 x 1, the 2 x 2 cluster as 2 x 2 x 1 over a (2 * tiles) x 2 grid.
+template <int BN_, int CL_, bool PAIR_, int RN_ = 1>
 struct Cfg {
-  static constexpr int BN = BN_;                // columns of C per cluster tile (MMA N)
+  static constexpr int BN = BN_;                // columns of C per CTA tile (MMA N)
   static constexpr int CL = CL_;                // CTAs per cluster
   static constexpr bool PAIR = PAIR_;
+  static constexpr int RN = RN_;                // CTAs along N
+  static constexpr int RM = CL / RN;            // CTAs along M
+  static constexpr int CLX = (RN == 1) ? CL : RN;   // launch cluster dimensions
+  static constexpr int CLY = CL / CLX;
   static constexpr bool MCAST = (CL > 1 && !PAIR);
+  static constexpr bool A_MCAST = MCAST && RN > 1;   // A shared along a cluster row
   static constexpr int CG = PAIR ? 2 : 1;       // tcgen05 cta_group
   static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns each CTA holds in shared memory
   static constexpr int MMA_M = PAIR ? 2 * BM : BM;
@@ -98,7 +110,8 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int B_BOXES = BN_CTA / 64;   // 64-column TMA boxes per stage
-  static constexpr int B_OWN_BOXES = MCAST ? B_BOXES / CL : B_BOXES;   // boxes this CTA loads
+  static constexpr int B_OWN_BOXES = MCAST ? B_BOXES / RM : B_BOXES;   // B boxes this CTA loads
+  static constexpr int A_OWN_ROWS = A_MCAST ? BM / RN : BM;            // A rows this CTA loads
   static constexpr int STAGES = FINE ? 9 : 6;
   // transaction bytes on the full barrier the MMA waits on: the pair's leader counts both
   // CTAs' loads; a multicast CTA receives its A and the whole B tile
@@ -125,29 +138,33 @@ struct Cfg {
   // consumer warps of a CLC response: TMA + 4 epilogue warps in every CTA, the MMA warp of
   // every CTA that issues MMAs, and the scheduler warp of rank 0
   static constexpr int CLC_CONSUMERS = 5 * CL + (PAIR ? 1 : CL) + 1;
-  static_assert(!PAIR || CL == 2, "CTA pairs only");
+  static_assert(!PAIR || (CL == 2 && RN == 1), "CTA pairs only");
+  static_assert(CL % RN == 0 && (RN == 1 || (RN == 2 && CL == 4)), "cluster shape");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % EPI_CHUNK == 0 && BN_CTA % 64 == 0 && BK % UMMA_K == 0, "tile shape");
-  static_assert(B_BOXES % (MCAST ? CL : 1) == 0, "B boxes split evenly over the cluster");
+  static_assert(B_BOXES % (MCAST ? RM : 1) == 0, "B boxes split evenly over a cluster column");
+  static_assert((A_OWN_ROWS * A_ROW) % 1024 == 0, "A halves start on a swizzle atom");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && C_BUF_BYTES % 1024 == 0, "1 KiB alignment");
 };
 
 // Host view of a shape's TMA boxes and k-slice depth.
 struct ShapeInfo {
   int bk;          // k per stage (A box width, B box height)
+  int a_rows;      // A box height (rows of A one CTA loads per stage)
   int epi_chunk;   // C box width (fp32 columns)
   int a_swizzle;   // bytes: 64 or 128
   int c_swizzle;   // bytes: 64 or 128
   int smem;
 };
 
-template <int BN, int CL, bool PAIR>
+template <int BN, int CL, bool PAIR, int RN = 1>
 constexpr ShapeInfo shape_info_of() {
-  using C = Cfg<BN, CL, PAIR>;
-  return ShapeInfo{C::BK, C::EPI_CHUNK, C::A_ROW, C::C_ROW, C::SMEM_BYTES};
+  using C = Cfg<BN, CL, PAIR, RN>;
+  return ShapeInfo{C::BK, C::A_OWN_ROWS, C::EPI_CHUNK, C::A_ROW, C::C_ROW, C::SMEM_BYTES};
 }
 
-inline ShapeInfo shape_info(int bn, int cl, bool pair) {
+inline ShapeInfo shape_info(int bn, int cl, bool pair, int rn = 1) {
+  if (cl == 4 && rn == 2) return shape_info_of<256, 4, false, 2>();
   if (cl == 2 && pair) return shape_info_of<256, 2, true>();
   if (cl == 2) return shape_info_of<256, 2, false>();
   if (cl == 4) return shape_info_of<256, 4, false>();
@@ -200,7 +217,7 @@ __device__ __forceinline__ void raster_map(int c, int mt, int nt, int group, int
   n = r / rows;
 }
 
-template <int CL>
+template <int CL, int RN>
 __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank) {
   Work w;
   w.c = c;
@@ -227,9 +244,11 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
   int m, n;
   raster_map(c - base, mt, nt, p.raster_group, m, n);
   w.g = g;
-  w.m_blk = m * CL + (int)rank;
-  w.n_blk = n;
-  w.pos = base * CL + w.m_blk * nt + n;
+  // rank r: row r / RN, column r % RN of the cluster tile; CTA tiles are numbered row-major
+  // over the problem's (mt * RM) x (nt * RN) grid, problems one after another
+  w.m_blk = m * (CL / RN) + (int)rank / RN;
+  w.n_blk = n * RN + (int)rank % RN;
+  w.pos = base * CL + w.m_blk * (nt * RN) + w.n_blk;
   w.kb = kb;
   return w;
 }
@@ -285,26 +304,26 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const Pa
 // ---------------------------------------------------------------- work iterator
 // Every role walks the same tile sequence.  In CLC mode each role consumes every response
 // of the ring (one release per consuming warp).
-template <int BN, int CL, bool PAIR, int SCHED>
+template <int BN, int CL, bool PAIR, int SCHED, int RN>
 struct WorkIter {
+  using C = Cfg<BN, CL, PAIR, RN>;
   int c = 0;
   int stage = 0;
   uint32_t phase = 0;
 
   __device__ __forceinline__ Work first(const Params& p, uint32_t rank) {
-    c = (int)(blockIdx.x / CL);
-    return make_work<CL>(p, c, rank);
+    c = (int)(blockIdx.x / C::CLX);
+    return make_work<CL, RN>(p, c, rank);
   }
 
   // `warp_wide`: all 32 lanes call (one release per warp); otherwise a single lane calls.
   __device__ __forceinline__ Work next(const Params& p, uint32_t rank, uint32_t smem_base, Ctl ctl,
                                        bool warp_wide) {
-    using C = Cfg<BN, CL, PAIR>;
     if constexpr (SCHED == SCHED_STATIC) {
-      c += (int)(gridDim.x / CL);
-      return make_work<CL>(p, c, rank);
+      c += (int)(gridDim.x / C::CLX);
+      return make_work<CL, RN>(p, c, rank);
     } else if constexpr (SCHED == SCHED_NONPERSISTENT) {
-      Work w = make_work<CL>(p, -1, rank);
+      Work w = make_work<CL, RN>(p, -1, rank);
       return w;
     } else {
       const uint32_t full = smem_base + C::OFF_BAR + 8 * (C::BAR_CLC_FULL + stage);
@@ -312,14 +331,14 @@ struct WorkIter {
       const uint32_t resp = smem_base + C::OFF_RESP + 16 * stage;
       volatile uint32_t* injected = reinterpret_cast<volatile uint32_t*>(
           __cvta_shared_to_generic(smem_base + C::OFF_MISC + 8 + 4 * stage));
-      Work w = make_work<CL>(p, -1, rank);
+      Work w = make_work<CL, RN>(p, -1, rank);
       const bool got = bar_wait<(CL > 1)>(full, phase, p, ctl, WAIT_CLC_FULL);
       if (got) {
         uint32_t x = 0;
         bool ok = false;
         if (*injected == 0) ok = clc_decode(resp, x);   // success predicate first
         fence_proxy_async_smem();                        // reads done before the slot is rewritten
-        if (ok) w = make_work<CL>(p, (int)(x / CL), rank);
+        if (ok) w = make_work<CL, RN>(p, (int)(x / C::CLX), rank);
       }
       if (warp_wide) __syncwarp();
       if (!warp_wide || lane_id() == 0) {
@@ -333,9 +352,9 @@ struct WorkIter {
 };
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, int CL, bool PAIR, int SCHED>
+template <int BN, int CL, bool PAIR, int SCHED, int RN = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<BN, CL, PAIR>;
+  using C = Cfg<BN, CL, PAIR, RN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -344,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t rank = (CL == 1) ? 0u : cluster_ctarank();
-  const int worker = (int)(blockIdx.x / CL);
+  const int worker = (int)(blockIdx.x / C::CLX);   // the cluster's launch id
 
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * (uint32_t)i; };
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
@@ -395,13 +414,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
-      WorkIter<BN, CL, PAIR, SCHED> it;
+      WorkIter<BN, CL, PAIR, SCHED, RN> it;
       Work w = it.first(p, rank);
       int s = 0;
       uint32_t ph = 0;
       int tile = 0;
       const uint32_t full0_leader = PAIR ? map_to_rank(bar(C::BAR_FULL), 0) : bar(C::BAR_FULL);
-      constexpr uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
+      const int rm = (int)rank / RN, rn = (int)rank % RN;   // place in the cluster tile
+      uint16_t col_ctas = 0;   // the CTAs of this cluster column share the B tile
+#pragma unroll
+      for (int r = 0; r < C::RM; ++r) col_ctas |= (uint16_t)(1u << (r * RN + rn));
+      // the CTAs of this cluster row share the A tile (2 x 2 clusters)
+      const uint16_t row_ctas = (uint16_t)(((1u << RN) - 1u) << (rm * RN));
       // throttle: one token per tile started; the scheduler issues fetch r only after token
       // r, so it fetches tile r + 1 once tile r - fetch_ahead has started (default: once tile
       // r has started, one tile ahead)
@@ -422,10 +446,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;
         const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
         const int ay = w.m_blk * BM;
+        const int a_row0 = ay + (C::A_MCAST ? rn * C::A_OWN_ROWS : 0);   // first A row this CTA loads
         const int bx = w.n_blk * BN + (PAIR ? (int)rank * C::BN_CTA : 0);
         const int pf = p.l2_prefetch;
         auto prefetch = [&](int kq) {
-          tma_prefetch_l2_2d(mA, kq * C::BK, ay);
+          tma_prefetch_l2_2d(mA, kq * C::BK, a_row0);
 #pragma unroll
           for (int j = 0; j < C::B_BOXES; ++j) tma_prefetch_l2_2d(mB, bx + 64 * j, kq * C::BK);
         };
@@ -445,12 +470,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
               tma_load_2d_pair(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
           } else {
             const uint32_t fb = bar(C::BAR_FULL + s);
-            tma_load_2d(a_dst, mA, fb, kb * C::BK, ay);
+            if constexpr (C::A_MCAST)   // this CTA's rows of the shared A tile, to its whole row
+              tma_load_2d_multicast(a_dst + (uint32_t)(rn * C::A_OWN_ROWS * C::A_ROW), mA, fb, kb * C::BK,
+                                    a_row0, row_ctas);
+            else
+              tma_load_2d(a_dst, mA, fb, kb * C::BK, ay);
 #pragma unroll
             for (int i = 0; i < C::B_OWN_BOXES; ++i) {
-              const int j = (int)rank * C::B_OWN_BOXES + i;   // this CTA's share of the B tile
+              const int j = rm * C::B_OWN_BOXES + i;   // this CTA's share of the B tile
               if constexpr (C::MCAST)
-                tma_load_2d_multicast(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK, all_ctas);
+                tma_load_2d_multicast(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK, col_ctas);
               else
                 tma_load_2d(b_dst + j * C::BK * 128, mB, fb, bx + 64 * j, kb * C::BK);
             }
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if ((!PAIR || rank == 0) && elect_one()) {
-      WorkIter<BN, CL, PAIR, SCHED> it;
+      WorkIter<BN, CL, PAIR, SCHED, RN> it;
       Work w = it.first(p, rank);
       int s = 0;
       uint32_t ph = 0;
@@ -550,7 +579,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if (misc[2 + s] == 0) ok = clc_decode(resp, x);
           fence_proxy_async_smem();
           if (ok && p.trace) {
-            const Work got = make_work<CL>(p, (int)(x / CL), 0);
+            const Work got = make_work<CL, RN>(p, (int)(x / C::CLX), 0);
             if (got.valid) p.trace[TRACE_WORDS * (size_t)got.pos + 5] = globaltimer() - t_issue;
           }
         }
@@ -563,7 +592,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - EPI_WARP0;   // TMEM lane quadrant (warp % 4)
-    WorkIter<BN, CL, PAIR, SCHED> it;
+    WorkIter<BN, CL, PAIR, SCHED, RN> it;
     Work w = it.first(p, rank);
     int acc = 0;
     uint32_t aph = 0;

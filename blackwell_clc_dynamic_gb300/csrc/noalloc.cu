@@ -107,10 +107,15 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   if (M < 0 || N < 0 || K < 0 || num_workers < 0) return GEMM_ERR_INVALID_ARG;
   if (sched != GEMM_SCHED_CLC && sched != GEMM_SCHED_STATIC && sched != GEMM_SCHED_NONPERSISTENT)
     return GEMM_ERR_INVALID_ARG;
-  if (tile.bm != 128 || tile.bk != 64 || cluster.y != 1 || cluster.z != 1) return GEMM_ERR_INVALID_ARG;
-  int bn = 0, cl = 0;
+  if (tile.bm != 128 || tile.bk != 64 || cluster.z != 1) return GEMM_ERR_INVALID_ARG;
+  int bn = 0, cl = 0, rn = 1;
   bool pair = false;   // clusters of 2 run the CTA-pair MMA (the default options)
-  if (cluster.x == 1 && (tile.bn == 128 || tile.bn == 256)) {
+  if (cluster.y != 1 && !(cluster.x == 2 && cluster.y == 2)) return GEMM_ERR_INVALID_ARG;
+  if (cluster.x == 2 && cluster.y == 2 && tile.bn == 256) {
+    bn = 256;
+    cl = 4;
+    rn = 2;
+  } else if (cluster.x == 1 && (tile.bn == 128 || tile.bn == 256)) {
     bn = tile.bn;
     cl = 1;
   } else if ((cluster.x == 2 || cluster.x == 4) && tile.bn == 256) {
@@ -133,8 +138,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   int rc = setup_device(dev);
   if (rc) return rc;
 
-  const int64_t mt = (M + (int64_t)BM * cl - 1) / ((int64_t)BM * cl);
-  const int64_t nt = (N + bn - 1) / bn;
+  const int64_t tile_m = (int64_t)BM * (cl / rn), tile_n = (int64_t)bn * rn;   // cluster tile
+  const int64_t mt = (M + tile_m - 1) / tile_m;
+  const int64_t nt = (N + tile_n - 1) / tile_n;
   const int64_t total = mt * nt;
   const int64_t n_tiles = total * cl;
   int64_t workers = total;
@@ -164,10 +170,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
 
   Params p;
   memset(&p, 0, sizeof p);
-  const ShapeInfo si = shape_info(bn, cl, pair);
+  const ShapeInfo si = shape_info(bn, cl, pair, rn);
   if (K > 0) {
     rc = encode(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
-                (uint32_t)si.bk, BM, si.a_swizzle);
+                (uint32_t)si.bk, (uint32_t)si.a_rows, si.a_swizzle);
     if (rc) return rc;
     rc = encode(&p.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64,
                 (uint32_t)si.bk, 128);
@@ -192,7 +198,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   p.inject_fail_after = -1;
 
   const int grid = (int)(workers * cl);
-  e = launch_any(bn, cl, pair, (int)sched, p, grid, s);
+  e = launch_any(bn, cl, pair, (int)sched, p, grid, s, rn);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

@@ -79,8 +79,14 @@ typedef enum {
  * computed by a CTA-pair MMA, or with gemm_opts_t.cluster_b_multicast by two 128 x 256
  * MMAs sharing B) and with cluster {4,1,1} (a 512 x 256 tile per cluster: four CTAs on
  * consecutive row blocks, each loading a quarter of the B tile and multicasting it to
- * the others).  A successful cancel takes a whole cluster; CTA rank r computes row block
- * r of the cluster tile.  bk must be 64; the library picks the k depth of its ring stages
+ * the others) and with cluster {2,2,1} (a 256 x 512 tile per cluster: four CTAs, each on
+ * one 128 x 256 quarter; the two CTAs of a row share their A tile and the two of a column
+ * their B tile, each loading half and multicasting it).  A successful cancel takes a
+ * whole cluster; with clusters {x,1,1} CTA rank r computes row block r of the cluster
+ * tile, with {2,2,1} rank r computes row block r / 2 and column block r % 2.  The cluster
+ * tiles of a problem (its rows and columns divided by the cluster tile's, rounded up) are
+ * numbered in raster order; that number is the launch coordinate of the cluster that owns
+ * the tile.  bk must be 64; the library picks the k depth of its ring stages
  * (32 when a CTA runs its own 128 x 256 MMA, which keeps nine stages in flight, 64
  * otherwise). */
 typedef struct { int bm, bn, bk; } gemm_tile_t;
@@ -211,8 +217,8 @@ CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
  *   claims[n_tiles]    how many times each CTA tile was computed (1 when correct;
  *                      counts saturate at 255)
  *   first[n_workers]   linear id of each worker's first tile, -1 if the worker never ran
- * CTA tiles are indexed row-major over (M / 128) x (N / bn) per problem, problems in
- * order.  Any output pointer may be NULL.  n_tiles / n_workers must equal the values
+ * CTA tiles are indexed row-major over (M / 128) x (N / bn) per problem (both rounded up
+ * to whole cluster tiles), problems in order.  Any output pointer may be NULL.  n_tiles / n_workers must equal the values
  * gemm_last_launch() reports.  On the device every entry carries a tag of the launch
  * that wrote it, so logging needs no clearing pass before a launch; this call keeps
  * only the entries of the most recent launch. */

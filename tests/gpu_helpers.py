@@ -32,17 +32,37 @@ def assert_close(C_gpu, C_ref, rel=1e-3):
     assert ok, f"max |dC| / (rel*(1+|C_ref|)) = {worst:.3g} (NaNs: {int(np.isnan(C_gpu).sum())})"
 
 
-def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8):
+def cluster_dims(cluster):
+    """(CTAs per cluster, CTAs along M, CTAs along N) of a cluster argument: an int or an
+    (x, y, z) tuple.  Clusters x by 1 stack their CTAs along M; the 2 x 2 cluster has x
+    CTAs along N and y along M."""
+    if isinstance(cluster, int):
+        return cluster, cluster, 1
+    x, y = int(cluster[0]), int(cluster[1])
+    if y == 1:
+        return x, x, 1
+    return x * y, y, x
+
+
+def grid_of(M, N, tile, cluster):
+    """(cluster-tile rows, cluster-tile columns, CTAs per cluster, CTAs along N)."""
+    cl, rm, rn = cluster_dims(cluster)
+    return math.ceil(M / (128 * rm)), math.ceil(N / (tile[1] * rn)), cl, rn
+
+
+def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8, rn=1):
     """(owner_lin, claims_lin) indexed by linear cluster-tile id, from CTA-tile logs.
-    tiles_m: cluster-tile rows of each problem (one entry for a plain problem); nt: tile
-    columns, one count for all problems or one per problem."""
+    tiles_m: cluster-tile rows of each problem (one entry for a plain problem); nt: cluster-
+    tile columns, one count for all problems or one per problem; rn: CTAs of a cluster
+    along N (CTA tiles are row-major over (tiles_m * cl / rn) x (nt * rn) per problem)."""
     owner_lin, claims_lin = [], []
     base = 0
+    rm = cl // rn
     nts = list(nt) if isinstance(nt, (list, tuple)) else [nt] * len(tiles_m)
     for mt, nt in zip(tiles_m, nts):
         for c in range(mt * nt):
             m, n = cv.raster(c, mt, nt, group_rows)
-            pos = [base * cl + (m * cl + r) * nt + n for r in range(cl)]
+            pos = [base * cl + (m * rm + r // rn) * (nt * rn) + n * rn + r % rn for r in range(cl)]
             ow = {int(owner[p]) for p in pos}
             assert len(ow) == 1, f"CTAs of one cluster tile logged different workers: {ow}"
             owner_lin.append(ow.pop())
@@ -52,10 +72,10 @@ def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8):
     return owner_lin, claims_lin
 
 
-def check_log(g, mode, tiles_m, nt, cl, num_workers=None):
+def check_log(g, mode, tiles_m, nt, cl, num_workers=None, rn=1):
     owner, claims, first = g.get_log()
     info = g.last_launch()
-    owner_lin, claims_lin = linear_log(owner, claims, tiles_m, nt, cl)
+    owner_lin, claims_lin = linear_log(owner, claims, tiles_m, nt, cl, rn=rn)
     assert len(owner_lin) == info["n_cluster_tiles"]
     cv.check_device_log(mode, owner_lin, claims_lin, first.tolist(), info["n_workers"], n_workers=num_workers)
     return owner_lin, first

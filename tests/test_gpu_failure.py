@@ -12,17 +12,18 @@ import torch
 
 import oracle
 import workloads as wl
-from tests.gpu_helpers import TILE_256, assert_close, check_log
+from tests.gpu_helpers import TILE_256, assert_close, check_log, cluster_dims
 
 pytestmark = pytest.mark.gpu
 
 WAIT_CLC_FULL = 5
 
 
-@pytest.mark.parametrize("cl,mc", [(1, 0), (2, 0), (4, 0)], ids=["c1", "c2pair", "c4mc"])
+@pytest.mark.parametrize("cl,mc", [(1, 0), (2, 0), (4, 0), ((2, 2, 1), 0)], ids=["c1", "c2pair", "c4mc", "c2x2"])
 def test_response_wait_times_out_and_is_reported(cl, mc):
     import blackwell_clc_dynamic_gb300 as m
-    M, N, K = 128 * cl * 6, 512, 256
+    ncta, rm, rn = cluster_dims(cl)
+    M, N, K = 128 * rm * 6, 512 * rn, 256
     A = wl.make_matrix((M, K), 101)
     B = wl.make_matrix((K, N), 102)
     with m.Gemm(0, timeout_ns=50_000_000, hold_scheduler=True, cluster_b_multicast=mc) as g:
@@ -36,7 +37,7 @@ def test_response_wait_times_out_and_is_reported(cl, mc):
         assert ei.value.code == m.GEMM_ERR_TIMEOUT
         # nothing was stolen: every launch computed its own tile, exactly once
         assert_close(C.cpu().numpy(), oracle.gemm(A, B))
-        owner_lin, first = check_log(g, "nonpersistent", [6], 2, cl)
+        owner_lin, first = check_log(g, "nonpersistent", [6], 2, ncta, rn=rn)
         # the error word was cleared by gemm_sync, and the context still works
         g.set_opts(hold_scheduler=0, timeout_ns=0)
         C2 = torch.full((M, N), float("nan"), device="cuda")

@@ -9,14 +9,17 @@ import torch
 import oracle
 import workloads as wl
 from oracle import coverage as cv
-from tests.gpu_helpers import TILE_128, TILE_256, assert_close, check_log, cluster_rows, run
+from tests.gpu_helpers import TILE_128, TILE_256, assert_close, check_log, cluster_dims, grid_of, run
 
 pytestmark = pytest.mark.gpu
 
 MODES = ["clc", "static", "nonpersistent"]
-# (tile, cluster size, B multicast): one CTA; CTA pair; clusters of 2 and 4 sharing B
-SHAPES = [(TILE_256, 1, 0), (TILE_128, 1, 0), (TILE_256, 2, 0), (TILE_256, 2, 1), (TILE_256, 4, 0)]
-SHAPE_IDS = ["n256c1", "n128c1", "n256c2", "n256c2mc", "n256c4mc"]
+# (tile, cluster, B multicast): one CTA; CTA pair; clusters of 2 and 4 sharing B; 2 x 2
+# clusters sharing A along rows and B along columns
+C2X2 = (2, 2, 1)
+SHAPES = [(TILE_256, 1, 0), (TILE_128, 1, 0), (TILE_256, 2, 0), (TILE_256, 2, 1), (TILE_256, 4, 0),
+          (TILE_256, C2X2, 0)]
+SHAPE_IDS = ["n256c1", "n128c1", "n256c2", "n256c2mc", "n256c4mc", "n256c2x2"]
 
 
 @pytest.fixture(scope="module")
@@ -71,9 +74,8 @@ def test_uniform_ragged_tail(g, tile, cl, mc, mode):
     B = wl.make_matrix((K, N), 22)
     C = run(g, A, B, tile=tile, cluster=cl, sched=mode, num_workers=5)
     assert_close(C, oracle.gemm(A, B))
-    mt = cluster_rows(M, cl)
-    nt = math.ceil(N / tile[1])
-    check_log(g, mode, [mt], nt, cl, num_workers=5 if mode == "static" else None)
+    mt, nt, ncta, rn = grid_of(M, N, tile, cl)
+    check_log(g, mode, [mt], nt, ncta, num_workers=5 if mode == "static" else None, rn=rn)
 
 
 def test_identity_and_rank_one(g):
@@ -231,8 +233,10 @@ def test_grouped_small(g, tile, cl, mc):
             for a, b, c in zip(As, Bs, dC):
                 if a.shape[0]:
                     assert_close(c.cpu().numpy(), oracle.gemm(a, b))
-            tiles_m = [math.ceil(m / (128 * cl)) for m in Ms]
-            check_log(g, mode, tiles_m, math.ceil(N / tile[1]), cl, num_workers=3 if mode == "static" else None)
+            grids = [grid_of(m, N, tile, cl) for m in Ms]
+            ncta, rn = grids[0][2], grids[0][3]
+            check_log(g, mode, [gr[0] for gr in grids], grids[0][1], ncta,
+                      num_workers=3 if mode == "static" else None, rn=rn)
 
 
 def test_run_host_matches_device_run(g):
@@ -361,9 +365,9 @@ def test_grouped_varied_shapes_small(g, tile, cl, mc, mode):
         if m and n:
             ref = oracle.gemm(a, b) if k else np.zeros((m, n))
             assert_close(c.cpu().numpy(), ref)
-    live = [(m, n) for m, n, k in shapes if m and n]
-    check_log(g, mode, [math.ceil(m / (128 * cl)) for m, n in live], [math.ceil(n / tile[1]) for m, n in live], cl,
-              num_workers=3 if mode == "static" else None)
+    grids = [grid_of(m, n, tile, cl) for m, n, k in shapes if m and n]
+    check_log(g, mode, [gr[0] for gr in grids], [gr[1] for gr in grids], grids[0][2],
+              num_workers=3 if mode == "static" else None, rn=grids[0][3])
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -408,7 +412,7 @@ def test_randomized_shapes_and_modes(g):
     """24 seeded random problems: ragged M, N, K (multiples of 8 where the ABI needs it),
     every schedule and cluster shape, integer inputs so the result must be bit-exact."""
     rng = np.random.default_rng(2024)
-    configs = [(TILE_256, 1, 0), (TILE_128, 1, 0), (TILE_256, 2, 0), (TILE_256, 2, 1), (TILE_256, 4, 0)]
+    configs = list(SHAPES)
     try:
         for i in range(24):
             tile, cl, mcast = configs[i % len(configs)]
@@ -426,31 +430,36 @@ def test_randomized_shapes_and_modes(g):
         g.set_opts(cluster_b_multicast=0, raster_group=8)
 
 
-@pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0)], ids=["pair", "c2_shared_b", "c4_shared_b"])
+@pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0), (C2X2, 0)],
+                         ids=["pair", "c2_shared_b", "c4_shared_b", "c2x2_shared_ab"])
 def test_square_full_size_cluster_modes(g, cl, mcast):
     """The square workload in the cluster launch configurations the benchmark times beside
     the headline (CLC): sampled elements and whole tiles against the oracle, exact log."""
     w = wl.SQUARE
     A, B = _inputs(w)
+    mt, nt, ncta, rn = grid_of(w.M, w.N, TILE_256, cl)
+    tm, tn = 128 * ncta // rn, 256 * rn   # cluster tile
     g.set_opts(cluster_b_multicast=mcast)
     try:
         C = torch.full((w.M, w.N), float("nan"), device="cuda")
         g.run(A.cuda(), B.cuda(), C, cluster=cl, sched="clc")
         g.sync()
-        _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(20 + cl + mcast),
-                       blocks=[(0, 128 * cl, 0, 256), (w.M - 128 * cl, w.M, w.N - 256, w.N)])
-        check_log(g, "clc", [w.M // (128 * cl)], w.N // 256, cl)
+        _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(20 + ncta + rn + mcast),
+                       blocks=[(0, tm, 0, tn), (w.M - tm, w.M, w.N - tn, w.N)])
+        check_log(g, "clc", [mt], nt, ncta, rn=rn)
     finally:
         g.set_opts(cluster_b_multicast=0)
 
 
-@pytest.mark.parametrize("cl,mcast,mode", [(1, 0, "clc"), (1, 0, "static"), (2, 0, "clc"), (4, 0, "clc")],
-                         ids=["c1-clc", "c1-static", "pair-clc", "c4-clc"])
+@pytest.mark.parametrize("cl,mcast,mode", [(1, 0, "clc"), (1, 0, "static"), (2, 0, "clc"), (4, 0, "clc"),
+                                           (C2X2, 0, "clc")],
+                         ids=["c1-clc", "c1-static", "pair-clc", "c4-clc", "c2x2-clc"])
 def test_trace_is_consistent_with_the_log(g, cl, mcast, mode):
     """Per tile: producer start <= last MMA issued <= epilogue start <= last store issued;
     the SM id is below the SM count; the worker is the one the ownership log names; CLC
     round trips are recorded only for tiles that came from a cancel."""
-    M, N, K = 128 * cl * 40, 512, 1024
+    ncta, rm, rn = cluster_dims(cl)
+    M, N, K = 128 * rm * 40, 512, 1024
     A = wl.make_matrix((M, K), 151)
     B = wl.make_matrix((K, N), 152)
     g.set_opts(trace_enable=1, cluster_b_multicast=mcast)
@@ -464,10 +473,11 @@ def test_trace_is_consistent_with_the_log(g, cl, mcast, mode):
     start, end, sm, worker, wait, rt, epi, last_mma = (tr[:, i] for i in range(8))
     assert np.all(start > 0) and np.all(end >= start) and np.all(epi >= start) and np.all(end >= epi)
     # CTA tiles are row-major over (M/128) x (N/256); the CTA of rank r holds row block
-    # cl*m + r.  The MMA time is recorded by the CTA that issues the MMA: every CTA, or
-    # rank 0 of a CTA pair.
-    rank = (np.arange(len(tr)) // (N // 256)) % cl
-    issuer = np.ones(len(tr), dtype=bool) if (cl == 1 or mcast or cl == 4) else rank == 0
+    # rm*m + r // rn and column block rn*n + r % rn.  The MMA time is recorded by the CTA
+    # that issues the MMA: every CTA, or rank 0 of a CTA pair.
+    pos = np.arange(len(tr))
+    rank = ((pos // (N // 256)) % rm) * rn + (pos % (N // 256)) % rn
+    issuer = np.ones(len(tr), dtype=bool) if (ncta == 1 or mcast or ncta == 4) else rank == 0
     assert np.all(last_mma[issuer] >= start[issuer]) and np.all(epi[issuer] >= last_mma[issuer])
     assert np.all(sm < g.sm_count)
     assert np.array_equal(worker, owner.astype(np.int64))
@@ -480,11 +490,12 @@ def test_trace_is_consistent_with_the_log(g, cl, mcast, mode):
 
 
 @pytest.mark.parametrize("ahead", [1, 2])
-@pytest.mark.parametrize("cl", [1, 2])
+@pytest.mark.parametrize("cl", [1, 2, C2X2], ids=["c1", "pair", "c2x2"])
 def test_fetch_ahead_keeps_coverage(g, ahead, cl):
     """With extra throttle tokens a worker holds up to 1 + ahead fetched tiles; results and
     coverage do not change."""
-    M, N, K = 128 * cl * 50, 512, 512
+    ncta, rm, rn = cluster_dims(cl)
+    M, N, K = 128 * rm * 50, 512 * rn, 512
     A = wl.make_matrix((M, K), 181, "int")
     B = wl.make_matrix((K, N), 182, "int")
     g.set_opts(fetch_ahead=ahead)
@@ -493,4 +504,4 @@ def test_fetch_ahead_keeps_coverage(g, ahead, cl):
     finally:
         g.set_opts(fetch_ahead=0)
     assert np.array_equal(C.astype(np.float64), oracle.gemm(A, B))
-    check_log(g, "clc", [50], 2, cl)
+    check_log(g, "clc", [50], 2, ncta, rn=rn)
