@@ -33,6 +33,7 @@ def test_noalloc_matches_gemm_run_on_two_calls():
         # second, so stale scratch from call 1 would show up in call 2
         (1000, 776, 1000, (128, 256, 64), 1, "clc", 91),
         (384, 512, 256, (128, 128, 64), 1, "static", 92),
+        (1000, 776, 1000, (128, 256, 64), (2, 2, 1), "clc", 93),
     ]
     with m.Gemm(0) as g:
         for M, N, K, tile, cl, sched, seed in cases:
