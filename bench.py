@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--all-out", default="bench_all.json", help="where --all writes its JSON")
     ap.add_argument("--all-steps", type=int, default=60)
     ap.add_argument("--workload", default="square", help="square | pair | grouped | grouped_vk | tail<T> | tiny")
-    ap.add_argument("--raster-group", type=int, default=8)
+    ap.add_argument("--raster-group", type=int, default=16)
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="k-blocks prefetched into L2 (-1: library default)")
     ap.add_argument("--occupy", type=int, default=0, help="SMs held by an occupier kernel while timing")
     ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent,pdl,clusters",

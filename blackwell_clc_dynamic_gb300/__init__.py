@@ -237,7 +237,7 @@ class Gemm:
     """One library handle on one device."""
 
     def __init__(self, device: int = 0, log: bool = True, trace: bool = False, timeout_ns: int = 0,
-                 inject_fail_after: int = -1, raster_group: int = 8, l2_prefetch: int = -1,
+                 inject_fail_after: int = -1, raster_group: int = 16, l2_prefetch: int = -1,
                  hold_scheduler: bool = False, cluster_b_multicast: bool = False, pdl: bool = False,
                  fetch_ahead: int = 0):
         self.opts = gemm_opts_t(int(log), int(trace), int(timeout_ns), int(inject_fail_after), int(raster_group),

@@ -32,6 +32,11 @@ constexpr int CLC_DEPTH = 3;     // response ring depth
 constexpr int THR_DEPTH = 3;     // throttle ring depth
 constexpr int EPI_WARP0 = 4;
 constexpr int TRACE_WORDS = 8;   // u64 per CTA tile in the optional trace
+// Default raster band height in tile rows.  Against 8-row bands, 16-row bands let the
+// tiles running at one time span half as many B columns, so B streams from DRAM half as
+// often; the work per SM clock is the same, but under the 1.4 kW power cap the SMs clock
+// higher (square 8192^3: +3-8 %; pair, grouped and tail shapes equal or slightly faster).
+constexpr int kDefaultRasterGroup = 16;
 
 // Device error word: [0] bits, [1] first failing wait site, [2] block of that wait.
 enum : int { ERRB_TIMEOUT = 1 };

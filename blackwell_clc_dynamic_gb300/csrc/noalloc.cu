@@ -187,7 +187,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   p.nt = (int)nt;
   p.total = (int)total;
   p.k_blocks = (int)((K + si.bk - 1) / si.bk);
-  p.raster_group = 8;
+  p.raster_group = kDefaultRasterGroup;
   p.log_owner = owner;
   p.log_claims = claims;
   p.log_first = first;

@@ -99,7 +99,7 @@ typedef struct {
     int     inject_fail_after; /* CLC test hook: after this many successful fetches the
                                   scheduler reports a failed fetch without issuing a cancel;
                                   < 0 (default) disables it */
-    int     raster_group;      /* tile rows per raster band; <= 0 selects 8; 1 = row-major */
+    int     raster_group;      /* tile rows per raster band; <= 0 selects 16; 1 = row-major */
     int     l2_prefetch;       /* k-blocks (of 64) the producer prefetches into L2 ahead of its
                                   loads; 0 = off (default), < 0 selects the default */
     int     hold_scheduler;    /* test hook (default 0): in CLC mode the scheduler issues no

@@ -75,7 +75,7 @@ def linear_log(owner, claims, tiles_m, nt, cl, group_rows=8, rn=1):
 def check_log(g, mode, tiles_m, nt, cl, num_workers=None, rn=1):
     owner, claims, first = g.get_log()
     info = g.last_launch()
-    owner_lin, claims_lin = linear_log(owner, claims, tiles_m, nt, cl, rn=rn)
+    owner_lin, claims_lin = linear_log(owner, claims, tiles_m, nt, cl, group_rows=g.opts.raster_group, rn=rn)
     assert len(owner_lin) == info["n_cluster_tiles"]
     cv.check_device_log(mode, owner_lin, claims_lin, first.tolist(), info["n_workers"], n_workers=num_workers)
     return owner_lin, first

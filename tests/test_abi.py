@@ -53,7 +53,7 @@ def test_strerror_and_version(pkg):
 def test_opts_default(pkg):
     o = pkg.gemm_opts_default()
     assert (o.log_enable, o.trace_enable, o.timeout_ns, o.inject_fail_after, o.raster_group, o.l2_prefetch,
-            o.hold_scheduler, o.cluster_b_multicast, o.pdl, o.fetch_ahead) == (1, 0, 2_000_000_000, -1, 8, 0, 0, 0, 0, 0)
+            o.hold_scheduler, o.cluster_b_multicast, o.pdl, o.fetch_ahead) == (1, 0, 2_000_000_000, -1, 16, 0, 0, 0, 0, 0)
 
 
 def test_create_without_gpu_reports_no_device(pkg):

@@ -11,13 +11,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def test_traffic_record_matches_only_its_capture(monkeypatch):
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     key = "gemm_n256_c1_clc_square"
+    rg = rec["kernels"][key]["raster_group"]
+    other = 8 if rg != 8 else 16
     monkeypatch.setattr(bench, "kernel_hash", lambda: rec["kernel_hash"])
-    assert bench.traffic_for(key, 8, 0) == float(rec["kernels"][key]["dram_bytes_per_launch"])
-    assert bench.traffic_for(key, 16, 0) is None          # other raster band
-    assert bench.traffic_for(key, 8, 4) is None           # other prefetch distance
-    assert bench.traffic_for("no_such_kernel", 8, 0) is None
+    assert bench.traffic_for(key, rg, 0) == float(rec["kernels"][key]["dram_bytes_per_launch"])
+    assert bench.traffic_for(key, other, 0) is None       # other raster band
+    assert bench.traffic_for(key, rg, 4) is None          # other prefetch distance
+    assert bench.traffic_for("no_such_kernel", rg, 0) is None
     monkeypatch.setattr(bench, "kernel_hash", lambda: "0" * 16)
-    assert bench.traffic_for(key, 8, 0) is None           # kernel changed since the capture
+    assert bench.traffic_for(key, rg, 0) is None          # kernel changed since the capture
 
 
 def test_clock_sampler_parses_nvidia_smi_lines():

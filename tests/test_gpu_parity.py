@@ -427,7 +427,7 @@ def test_randomized_shapes_and_modes(g):
             ref = oracle.gemm(A, B) if K else np.zeros((M, N))
             assert np.array_equal(C.astype(np.float64), ref), (i, M, N, K, tile, cl, mcast, mode)
     finally:
-        g.set_opts(cluster_b_multicast=0, raster_group=8)
+        g.set_opts(cluster_b_multicast=0, raster_group=16)
 
 
 @pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0), (C2X2, 0)],
