@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -36,7 +37,7 @@ METRIC = "GEMM TFLOP/s & % of bf16 dense peak (CLC vs static vs non-persistent) 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # files whose change invalidates the committed DRAM-traffic counters
 KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh", "launch.cuh", "kern_n128_c1.cu", "kern_n256_c1.cu", "kern_n256_c2.cu",
-                  "kern_n256_c2mc.cu", "kern_n256_c4mc.cu"]
+                  "kern_n256_c2mc.cu", "kern_n256_c4mc.cu", "kern_n256_c2x2.cu"]
 
 
 def parse():
@@ -81,11 +82,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed: a comment edit does not
+    change the kernel a traffic record was captured on."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blackwell_clc_dynamic_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

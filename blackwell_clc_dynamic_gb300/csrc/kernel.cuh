@@ -1,9 +1,11 @@
 // Warp-specialised, output-tile-scheduled bf16 GEMM for sm_103a (C = A * B, fp32 out).
 //
 // One CTA (or CTA pair) computes one output tile at a time:
-//   warp 0      TMA producer: A[128 x 64] and B[64 x BN/CL] k-slices into a swizzled ring
-//   warp 1      MMA issuer (CTA rank 0): tcgen05.mma kind::f16 into a double-buffered TMEM
-//               accumulator; also allocates / frees tensor memory
+//   warp 0      TMA producer: A[128 x BK] and B[BK x BN] k-slices (BK = 32 or 64) into a
+//               swizzled ring; in multicast clusters each CTA loads its share of the tiles
+//               its cluster row / column shares and multicasts it
+//   warp 1      MMA issuer (every CTA; only rank 0 of a CTA pair): tcgen05.mma kind::f16
+//               into a double-buffered TMEM accumulator; also allocates / frees tensor memory
 //   warp 2      CLC scheduler (CTA rank 0, CLC mode only): try_cancel into a 3-deep ring of
 //               16-byte responses, bounded by a throttle pipeline
 //   warp 3      spare
@@ -46,13 +48,13 @@ enum : int {
 };
 
 struct Params {
-  CUtensorMap tmA;               // A: bf16 M x K row-major, box 64 x 128, 128B swizzle
-  CUtensorMap tmB;               // B: bf16 K x N row-major, box 64(n) x 64(k), 128B swizzle
-  CUtensorMap tmC;               // C: fp32 M x N row-major, box 32 x 32, 128B swizzle
+  CUtensorMap tmA;               // A: bf16 M x K row-major, box BK(k) x A_OWN_ROWS, swizzle = BK * 2 bytes
+  CUtensorMap tmB;               // B: bf16 K x N row-major, box 64(n) x BK(k), 128B swizzle
+  CUtensorMap tmC;               // C: fp32 M x N row-major, box EPI_CHUNK x 32, swizzle = EPI_CHUNK * 4 bytes
   const CUtensorMap* gmaps;      // grouped: (A, B, C) per problem in device memory
   const int* g_tile_start;       // grouped: G+1 prefix sums of cluster tiles
   const int* g_mt;               // grouped: cluster-tile rows of each problem
-  const int* g_nt;               // grouped: tile columns of each problem
+  const int* g_nt;               // grouped: cluster-tile columns of each problem
   const int* g_kb;               // grouped: k-blocks (ceil(K_g / BK)) of each problem
   int G;                         // number of problems (0: plain problem in tmA/tmB/tmC)
   int mt, nt;                    // cluster-tile grid of the plain problem
