@@ -221,16 +221,19 @@ CLCGEMM_API int gemm_last_launch(gemm_handle_t h, gemm_launch_info_t *info);
  * to whole cluster tiles), problems in order.  Any output pointer may be NULL.  n_tiles / n_workers must equal the values
  * gemm_last_launch() reports.  On the device every entry carries a tag of the launch
  * that wrote it, so logging needs no clearing pass before a launch; this call keeps
- * only the entries of the most recent launch. */
+ * only the entries of the most recent launch.  GEMM_ERR_INVALID_ARG if the most recent
+ * launch wrote no log (log_enable was 0 when it ran, or nothing was launched). */
 CLCGEMM_API int gemm_get_log(gemm_handle_t h, int32_t *owner, int32_t *claims, int32_t *first,
                  int64_t n_tiles, int64_t n_workers);
 
-/* gemm_get_trace: copy-out of the trace of the most recent run, waiting for its stream (requires
- * trace_enable): 8 x uint64 per CTA tile (out holds n_tiles * 8):
+/* gemm_get_trace: copy-out of the trace of the most recent run, waiting for its stream (that
+ * run must have had trace_enable set; GEMM_ERR_INVALID_ARG otherwise): 8 x uint64 per CTA
+ * tile (out holds n_tiles * 8):
  *   [0] start ns (the producer begins the tile; device globaltimer)  [1] end ns (the
  *   epilogue issued the tile's last store)  [2] SM id  [3] worker  [4] ns the producer
- *   waited for the CLC response that named this tile (0 for a worker's first tile and
- *   for the other schedules)  [5] ns from the try_cancel that returned this tile to the
+ *   spent obtaining this tile after finishing the loads of its previous one (CLC: waiting
+ *   for the response that named it; static: its next-tile arithmetic; 0 for a worker's
+ *   first tile)  [5] ns from the try_cancel that returned this tile to the
  *   scheduler seeing its response (CLC, rank-0 tile only)  [6] ns when the epilogue saw
  *   the finished accumulator  [7] ns when the MMA warp issued the tile's last MMA
  *   (rank 0 for CTA pairs). */

@@ -163,6 +163,8 @@ def test_log_keeps_only_the_latest_launch():
         h.set_opts(log_enable=0)
         run(h, A, B, sched="clc")
         h.set_opts(log_enable=1)
+        with pytest.raises(m.GemmError):      # the most recent launch wrote no log
+            h.get_log()
         assert_close(run(h, a, b, sched="nonpersistent"), oracle.gemm(a, b))
         check_log(h, "nonpersistent", [2], 4, 1)
         assert_close(run(h, A, B, sched="clc"), oracle.gemm(A, B))
