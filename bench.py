@@ -90,6 +90,9 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
+TENSOR_FLOP_PER_SM_CLOCK = 8192   # dense bf16 tcgen05 rate of one SM
+
+
 def kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blackwell_clc_dynamic_gb300", "csrc")
@@ -445,6 +448,13 @@ def run_ours(args, ws, rank, local):
             "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
             "algorithmic_flops_per_launch": w.flops, "algorithmic_min_bytes_per_launch": w.min_bytes,
             "kernel": kname}
+    if clocks and clocks.get("sm_mhz"):
+        # the tensor pipe's own bound at the clock the SMs actually ran: 8192 dense bf16 flop
+        # per SM clock (one 128 x 256 x 16 MMA per 128 clocks), times the SMs, times the
+        # median SM clock sampled during the timed region
+        clock_peak = sms * TENSOR_FLOP_PER_SM_CLOCK * clocks["sm_mhz"] * 1e6 / 1e12
+        roof["clock_peak"] = clock_peak
+        roof["frac_of_clock_peak"] = achieved / clock_peak
     big = w.min_bytes > 129e6
     line = {
         "metric": METRIC, "value": clc_m["tflops"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
