@@ -408,7 +408,7 @@ def run_ours(args, ws, rank, local):
 
         def e2e_step():
             g.run_host(A, B, Ch, tile=tile, cluster=cl, sched="clc", stream=stream)
-        tot, per = time_steps(e2e_step, n_e2e, 2, stream, barrier, torch.cuda.synchronize)
+        tot, per = time_steps(e2e_step, n_e2e, 5, stream, barrier, torch.cuda.synchronize)
         g.sync(stream)
         tot = max_over_ranks(tot, ws)
         e2e = {"value": ws * n_e2e * w.flops / (tot * 1e-3) / 1e12, "unit": "TFLOP/s",
