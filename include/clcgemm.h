@@ -155,7 +155,9 @@ CLCGEMM_API int gemm_set_opts(gemm_handle_t h, const gemm_opts_t *opts);
  *   sched        gemm_sched_t
  *   num_workers  STATIC only: workers (clusters) to launch; 0 = SM count / cluster size.
  *                Ignored by CLC and NONPERSISTENT, which launch one cluster per tile.
- * Asynchronous; returns after the launch. */
+ * Asynchronous; returns after the launch.  A call may be captured into a CUDA graph once
+ * the handle has run the same shape outside the capture (so its workspace is allocated);
+ * capture with log_enable = 0: a replay reuses the log tag of the capture. */
 CLCGEMM_API int gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
              const void *A, const void *B, float *C,
              gemm_tile_t tile, gemm_cluster_t cluster, gemm_sched_t sched,
