@@ -434,7 +434,7 @@ def run_ours(args, ws, rank, local):
         return 0
 
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:     # the CPU baseline is reported at N = 1 only
         cpu = cpu_baseline(A, B, args.cpu_seconds)
 
     clc_m = modes["clc"]
