@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--raster-group", type=int, default=16)
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="k-blocks prefetched into L2 (-1: library default)")
     ap.add_argument("--occupy", type=int, default=0, help="SMs held by an occupier kernel while timing")
+    ap.add_argument("--trace-modes", action="store_true",
+                    help="one traced launch of every timed mode row (\"traced_modes\" in the JSON line)")
     ap.add_argument("--modes", default="clc,static_148,static_sms,nonpersistent,pdl,clusters",
                     help="comma-separated subset of the schedules to time (clc is always first)")
     return ap.parse_args()
@@ -418,6 +420,7 @@ def run_ours(args, ws, rank, local):
     # one traced launch per schedule (outside the timed region): how evenly the SMs finish
     # and what consuming CLC responses costs
     traced = {}
+    traced_modes = None
     if not args.occupy:
         for key, mode, nw in (("clc", "clc", 0), (f"static_{planned}", "static", planned)):
             st = trace_stats(g, step(mode, nw))
@@ -426,6 +429,14 @@ def run_ours(args, ws, rank, local):
                            "producer_wait_for_clc_response_us": st["producer_wait_for_clc_response"],
                            "try_cancel_round_trip_us": st["try_cancel_round_trip"],
                            "epilogue_us_mean": st["epilogue_us"]["mean_us"] if st["epilogue_us"] else None}
+        if args.trace_modes:
+            traced_modes = {}
+            for r in order:
+                g.set_opts(cluster_b_multicast=r["mcast"], pdl=r["pdl"], log_enable=r["log"])
+                try:
+                    traced_modes[r["key"]] = trace_stats(g, step(r["sched"], r["nw"], r["cl"]))
+                finally:
+                    g.set_opts(cluster_b_multicast=0, pdl=0, log_enable=1)
 
     if rank != 0:
         g.close()
@@ -473,6 +484,8 @@ def run_ours(args, ws, rank, local):
         "modes": modes, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches, "clocks": clocks, "traced_launch": traced,
     }
+    if traced_modes is not None:
+        line["traced_modes"] = traced_modes
     if args.occupy:
         line["occupier_hit_time_limit"] = bool(occ_status)
     emit(line, args)
