@@ -459,6 +459,17 @@ def run_ours(args, ws, rank, local):
             "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
             "algorithmic_flops_per_launch": w.flops, "algorithmic_min_bytes_per_launch": w.min_bytes,
             "kernel": kname}
+    ai = w.flops / w.min_bytes
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai < ridge:
+        # below the ridge (skinny shapes such as the tail sweep) the HBM roofline binds:
+        # algorithmic bytes (each operand read once, C written once) per launch / duration
+        gbs = w.min_bytes / (kernel_ms * 1e-3) / 1e9
+        roof.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "peak_kind": f"hbm_gbs ({peaks_src})",
+                     "tensor_frac_sustained": achieved / peaks["bf16_tflops_sustained"]})
+    roof["arithmetic_intensity"] = ai
+    roof["ridge_flop_per_byte"] = ridge
     if clocks and clocks.get("sm_mhz"):
         # the tensor pipe's own bound at the clock the SMs actually ran: 8192 dense bf16 flop
         # per SM clock (one 128 x 256 x 16 MMA per 128 clocks), times the SMs, times the
