@@ -507,3 +507,21 @@ def test_fetch_ahead_keeps_coverage(g, ahead, cl):
         g.set_opts(fetch_ahead=0)
     assert np.array_equal(C.astype(np.float64), oracle.gemm(A, B))
     check_log(g, "clc", [50], 2, ncta, rn=rn)
+
+
+@pytest.mark.parametrize("cl", [1, 2, C2X2], ids=["c1", "pair", "c2x2"])
+def test_l2_prefetch_option_keeps_results(g, cl):
+    """The optional L2 prefetch ahead of the ring (a hint: it moves no data into shared
+    memory) leaves results and coverage unchanged, ragged edges included."""
+    ncta, rm, rn = cluster_dims(cl)
+    M, N, K = 1000, 776, 2040
+    A = wl.make_matrix((M, K), 201, "int")
+    B = wl.make_matrix((K, N), 202, "int")
+    g.set_opts(l2_prefetch=8)
+    try:
+        C = run(g, A, B, cluster=cl, sched="clc")
+    finally:
+        g.set_opts(l2_prefetch=0)
+    assert np.array_equal(C.astype(np.float64), oracle.gemm(A, B))
+    mt, nt, ncta, rn = grid_of(M, N, TILE_256, cl)
+    check_log(g, "clc", [mt], nt, ncta, rn=rn)
