@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="--impl reference: CPU seconds for all warm-up and timed steps together")
     ap.add_argument("--settle-ms", type=float, default=1500.0,
                     help="untimed back-to-back launches before the first timed mode, so every mode is timed "
                          "at the same power and clock state")
@@ -194,7 +196,7 @@ def run_reference(args, ws, rank):
     w = wl.SQUARE
     A, B = wl.make_inputs(w)
     t_row = oracle_rows_rate(A, B, 2) / 2
-    budget = 90.0
+    budget = args.ref_seconds
     rows = max(1, int(budget / max(1, args.steps + args.warmup) / t_row))
     for _ in range(args.warmup):
         oracle.gemm_block(A, B, 0, rows, 0, w.N)
