@@ -4,6 +4,7 @@ import math
 import os
 import random
 
+import numpy as np
 import pytest
 
 from oracle import coverage as cv
@@ -150,3 +151,25 @@ def test_grouped_tile_per_problem_columns():
     assert out[5:] == [(2, 0, 0), (2, 1, 0), (2, 2, 0), (2, 0, 1), (2, 1, 1), (2, 2, 1)]
     # the same as the uniform form when every problem has the same column count
     assert [cv.grouped_tile(c, [2, 3], [4, 4]) for c in range(20)] == [cv.grouped_tile(c, [2, 3], 4) for c in range(20)]
+
+
+def test_greedy_schedules_respect_the_list_scheduling_bound():
+    """CLC (fetch when a tile ends) and non-persistent launches never leave a slot idle while
+    a tile is pending, so they are greedy list schedules: for tile costs c on R slots the
+    makespan lies between sum(c)/R and sum(c)/R + (1 - 1/R) max(c) (Graham's bound for list
+    scheduling).  Static scheduling is not greedy and may exceed it."""
+    rng = np.random.default_rng(17)
+    exceeded = 0
+    for _ in range(300):
+        T = int(rng.integers(1, 60))
+        R = int(rng.integers(1, 12))
+        cost = list(rng.uniform(0.1, 5.0, size=T))
+        lo, hi = sum(cost) / R, sum(cost) / R + (1 - 1 / R) * max(cost)
+        for mode in (cv.CLC, cv.NONPERSISTENT):
+            s = cv.simulate(T, mode, R, cost=cost)
+            cv.check_schedule(s)
+            assert lo - 1e-9 <= s.makespan <= hi + 1e-9, (mode, T, R, s.makespan, lo, hi)
+        st = cv.simulate(T, cv.STATIC, R, n_workers=R + int(rng.integers(0, 3)), cost=cost)
+        cv.check_schedule(st)
+        exceeded += st.makespan > hi + 1e-9
+    assert exceeded > 0, "static should exceed the greedy bound on some uneven draws"
