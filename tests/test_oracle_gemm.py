@@ -155,3 +155,16 @@ def test_block_against_numpy_int64():
     blk = oracle.gemm_block(a.to(torch.bfloat16), b.to(torch.bfloat16), 17, 61, 5, 83)
     ref = a.numpy().astype(np.int64)[17:61] @ b.numpy().astype(np.int64)[:, 5:83]
     assert np.array_equal(blk, ref.astype(np.float64))
+
+
+def test_transpose_identity_bit_exact():
+    """(A B)^T = B^T A^T: both sides sum the same exact products in ascending k, so the
+    oracle must return the transpose bit for bit (an i/j index swap anywhere breaks it)."""
+    import torch
+    rng = np.random.default_rng(21)
+    A = _rand_bits(rng, (37, 29))
+    B = _rand_bits(rng, (29, 45))
+    C = oracle.gemm(A, B)
+    At = torch.from_numpy(A.view(np.int16)).t().contiguous().view(torch.bfloat16)
+    Bt = torch.from_numpy(B.view(np.int16)).t().contiguous().view(torch.bfloat16)
+    assert np.array_equal(oracle.gemm(Bt, At), C.T)
