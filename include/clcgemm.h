@@ -141,7 +141,8 @@ CLCGEMM_API void gemm_opts_default(gemm_opts_t *opts);
  * device, GEMM_ERR_UNSUPPORTED_DEVICE when the device is not sm_103. */
 CLCGEMM_API int gemm_create(int device, const gemm_opts_t *opts, gemm_handle_t *out);
 
-/* gemm_destroy: synchronise the device and free the handle's workspace.  NULL is a no-op. */
+/* gemm_destroy: release the handle's SM occupier if it still runs, synchronise the device
+ * and free the handle's workspace.  NULL is a no-op. */
 CLCGEMM_API void gemm_destroy(gemm_handle_t h);
 
 /* gemm_set_opts: replace the handle's options (NULL = defaults). */
