@@ -39,6 +39,22 @@ cudaError_t launch_shape(int sched, const Params& p, int grid_ctas, cudaStream_t
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
+// Load the three schedule variants of a shape now and set their shared-memory limit.  With
+// CUDA's lazy module loading a kernel's code is loaded at its first launch, and that load
+// can wait until the device is idle: a first launch while another kernel holds SMs (an
+// occupier spinning on a host flag) would stall until that kernel ends.
+template <int BN, int CL, bool PAIR, int RN = 1>
+cudaError_t prepare_shape() {
+  constexpr int smem = Cfg<BN, CL, PAIR, RN>::SMEM_BYTES;
+  void (*ks[3])(const Params) = {gemm_kernel<BN, CL, PAIR, SCHED_CLC, RN>, gemm_kernel<BN, CL, PAIR, SCHED_STATIC, RN>,
+                                 gemm_kernel<BN, CL, PAIR, SCHED_NONPERSISTENT, RN>};
+  for (auto k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 template <int BN, int CL, bool PAIR, int RN = 1>
 cudaError_t max_clusters_shape(int* out) {
   using C = Cfg<BN, CL, PAIR, RN>;
@@ -75,6 +91,23 @@ cudaError_t max_clusters_n256_c2(int* out);
 cudaError_t max_clusters_n256_c2mc(int* out);
 cudaError_t max_clusters_n256_c4mc(int* out);
 cudaError_t max_clusters_n256_c2x2(int* out);
+cudaError_t prepare_n128_c1();
+cudaError_t prepare_n256_c1();
+cudaError_t prepare_n256_c2();
+cudaError_t prepare_n256_c2mc();
+cudaError_t prepare_n256_c4mc();
+cudaError_t prepare_n256_c2x2();
+
+// Load every kernel of the library on the current device (see prepare_shape).
+inline cudaError_t prepare_all() {
+  cudaError_t (*fs[])() = {prepare_n128_c1, prepare_n256_c1, prepare_n256_c2, prepare_n256_c2mc, prepare_n256_c4mc,
+                           prepare_n256_c2x2};
+  for (auto f : fs) {
+    cudaError_t e = f();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 // The launch function of a shape (nullptr if unsupported).
 inline cudaError_t launch_any(int bn, int cl, bool pair, int sched, const Params& p, int grid, cudaStream_t s,

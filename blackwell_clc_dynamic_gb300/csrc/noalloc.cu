@@ -79,6 +79,8 @@ int setup_device(int dev) {
   if (e != cudaSuccess) return from_cuda(e);
   if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
   void* p = nullptr;
+  e = prepare_all();   // load every kernel now rather than at a first launch
+  if (e != cudaSuccess) return from_cuda(e);
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess || p == nullptr) return from_cuda(e == cudaSuccess ? cudaErrorUnknown : e);
   g_scratch_dev[dev] = static_cast<int32_t*>(p);

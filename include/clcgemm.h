@@ -138,7 +138,10 @@ CLCGEMM_API void gemm_opts_default(gemm_opts_t *opts);
 
 /* gemm_create: open a handle on CUDA device `device` (makes it current on this thread).
  * opts may be NULL (defaults).  Fails with GEMM_ERR_NO_DEVICE when there is no usable
- * device, GEMM_ERR_UNSUPPORTED_DEVICE when the device is not sm_103. */
+ * device, GEMM_ERR_UNSUPPORTED_DEVICE when the device is not sm_103.  It loads every
+ * kernel of the library on the device, so that no later launch waits for code loading
+ * (under CUDA's lazy loading a first launch can wait until other kernels have finished,
+ * which never happens while the SM occupier waits for the host). */
 CLCGEMM_API int gemm_create(int device, const gemm_opts_t *opts, gemm_handle_t *out);
 
 /* gemm_destroy: release the handle's SM occupier if it still runs, synchronise the device
