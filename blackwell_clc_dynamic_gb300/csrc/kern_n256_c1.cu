@@ -6,5 +6,5 @@ cudaError_t launch_n256_c1(int sched, const Params& p, int grid_ctas, cudaStream
   return launch_shape<256, 1, false>(sched, p, grid_ctas, stream);
 }
 cudaError_t max_clusters_n256_c1(int* out) { return max_clusters_shape<256, 1, false>(out); }
-cudaError_t prepare_n256_c1() { return prepare_shape<256, 1, false>(); }
+cudaError_t warm_n256_c1(const Params& p0, cudaStream_t s) { return warm_shape<256, 1, false>(p0, s); }
 }  // namespace clcg

@@ -7,5 +7,5 @@ cudaError_t launch_n256_c2x2(int sched, const Params& p, int grid_ctas, cudaStre
   return launch_shape<256, 4, false, 2>(sched, p, grid_ctas, stream);
 }
 cudaError_t max_clusters_n256_c2x2(int* out) { return max_clusters_shape<256, 4, false, 2>(out); }
-cudaError_t prepare_n256_c2x2() { return prepare_shape<256, 4, false, 2>(); }
+cudaError_t warm_n256_c2x2(const Params& p0, cudaStream_t s) { return warm_shape<256, 4, false, 2>(p0, s); }
 }  // namespace clcg

@@ -2,6 +2,7 @@
 // tile / cluster shape so the library builds in parallel).
 #pragma once
 #include <cuda_runtime.h>
+#include <string.h>
 
 #include "kernel.cuh"
 
@@ -39,17 +40,15 @@ cudaError_t launch_shape(int sched, const Params& p, int grid_ctas, cudaStream_t
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-// Load the three schedule variants of a shape now and set their shared-memory limit.  With
-// CUDA's lazy module loading a kernel's code is loaded at its first launch, and that load
-// can wait until the device is idle: a first launch while another kernel holds SMs (an
-// occupier spinning on a host flag) would stall until that kernel ends.
+// Launch the three schedule variants of a shape once, over an empty problem (p0.total = 0:
+// every role finds no tile and the kernel exits).  Whatever a kernel's first launch costs
+// (under CUDA's lazy module loading it loads the code, and that can wait until the device
+// is idle) is paid here, not at a later launch that would wait for a kernel holding SMs,
+// such as the occupier spinning on a host flag.
 template <int BN, int CL, bool PAIR, int RN = 1>
-cudaError_t prepare_shape() {
-  constexpr int smem = Cfg<BN, CL, PAIR, RN>::SMEM_BYTES;
-  void (*ks[3])(const Params) = {gemm_kernel<BN, CL, PAIR, SCHED_CLC, RN>, gemm_kernel<BN, CL, PAIR, SCHED_STATIC, RN>,
-                                 gemm_kernel<BN, CL, PAIR, SCHED_NONPERSISTENT, RN>};
-  for (auto k : ks) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t warm_shape(const Params& p0, cudaStream_t s) {
+  for (int sched = SCHED_CLC; sched <= SCHED_NONPERSISTENT; ++sched) {
+    cudaError_t e = launch_shape<BN, CL, PAIR, RN>(sched, p0, CL, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -91,22 +90,31 @@ cudaError_t max_clusters_n256_c2(int* out);
 cudaError_t max_clusters_n256_c2mc(int* out);
 cudaError_t max_clusters_n256_c4mc(int* out);
 cudaError_t max_clusters_n256_c2x2(int* out);
-cudaError_t prepare_n128_c1();
-cudaError_t prepare_n256_c1();
-cudaError_t prepare_n256_c2();
-cudaError_t prepare_n256_c2mc();
-cudaError_t prepare_n256_c4mc();
-cudaError_t prepare_n256_c2x2();
+cudaError_t warm_n128_c1(const Params& p0, cudaStream_t s);
+cudaError_t warm_n256_c1(const Params& p0, cudaStream_t s);
+cudaError_t warm_n256_c2(const Params& p0, cudaStream_t s);
+cudaError_t warm_n256_c2mc(const Params& p0, cudaStream_t s);
+cudaError_t warm_n256_c4mc(const Params& p0, cudaStream_t s);
+cudaError_t warm_n256_c2x2(const Params& p0, cudaStream_t s);
 
-// Load every kernel of the library on the current device (see prepare_shape).
-inline cudaError_t prepare_all() {
-  cudaError_t (*fs[])() = {prepare_n128_c1, prepare_n256_c1, prepare_n256_c2, prepare_n256_c2mc, prepare_n256_c4mc,
-                           prepare_n256_c2x2};
+// Launch every kernel of the library once over an empty problem on stream `s` (see
+// warm_shape) and wait for them.  `err` receives device error words (none are expected).
+inline cudaError_t warm_all(int* err, cudaStream_t s) {
+  Params p0;
+  memset(&p0, 0, sizeof p0);
+  p0.total = 0;               // no tile: every role exits at once
+  p0.hold_scheduler = 1;      // and the CLC scheduler issues nothing
+  p0.raster_group = 1;
+  p0.err = err;
+  p0.timeout_ns = 2000000000LL;
+  p0.inject_fail_after = -1;
+  cudaError_t (*fs[])(const Params&, cudaStream_t) = {warm_n128_c1, warm_n256_c1, warm_n256_c2, warm_n256_c2mc,
+                                                       warm_n256_c4mc, warm_n256_c2x2};
   for (auto f : fs) {
-    cudaError_t e = f();
+    cudaError_t e = f(p0, s);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;
+  return cudaStreamSynchronize(s);
 }
 
 // The launch function of a shape (nullptr if unsupported).

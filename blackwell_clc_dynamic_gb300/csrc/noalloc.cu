@@ -79,10 +79,16 @@ int setup_device(int dev) {
   if (e != cudaSuccess) return from_cuda(e);
   if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
   void* p = nullptr;
-  e = prepare_all();   // load every kernel now rather than at a first launch
-  if (e != cudaSuccess) return from_cuda(e);
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess || p == nullptr) return from_cuda(e == cudaSuccess ? cudaErrorUnknown : e);
+  // launch every kernel once over an empty problem now, rather than have a first launch
+  // load code later (see warm_all); the error words of the scratch take any report
+  cudaStream_t st = nullptr;
+  e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = warm_all(static_cast<int32_t*>(p), st);
+  cudaStreamDestroy(st);
+  if (e != cudaSuccess) return from_cuda(e);
   g_scratch_dev[dev] = static_cast<int32_t*>(p);
   g_sms[dev] = sms;
   return GEMM_OK;
