@@ -4,8 +4,10 @@ Under CUDA's lazy module loading a kernel's code is loaded at its first launch, 
 load can wait until the device is idle.  While the SM occupier spins on a host flag, such
 a wait would last until the occupier's time limit.  gemm_create loads every kernel of the
 library up front; this test runs in a fresh process with lazy loading forced on, starts
-the occupier after one CLC launch and then makes first launches of other kernels.  A
-regression is bounded: the occupier releases its SMs after its 20 s limit."""
+the occupier after one CLC launch and then makes first launches of other kernels, each
+within the workspace the CLC launch sized (growing it synchronises the device, which
+would wait for the occupier by design).  A regression is bounded: the occupier releases
+its SMs after its 20 s limit."""
 import os
 import subprocess
 import sys
@@ -32,7 +34,7 @@ s.synchronize()
 g.occupy_start(24, limit_ns=20_000_000_000, stream=so)
 g.occupy_wait_resident(10_000)
 t0 = time.perf_counter()
-g.run(A, B, C, sched="static", num_workers=148, stream=s)
+g.run(A, B, C, sched="static", num_workers=64, stream=s)   # within the sized workspace
 g.run(A, B, C, sched="nonpersistent", stream=s)
 g.run(A, B, C, cluster=2, stream=s)
 g.run(A, B, C, cluster=(2, 2, 1), stream=s)
