@@ -36,8 +36,9 @@ sys.path.insert(0, ROOT)
 METRIC = "GEMM TFLOP/s & % of bf16 dense peak (CLC vs static vs non-persistent) at 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # files whose change invalidates the committed DRAM-traffic counters
-KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh", "launch.cuh", "kern_n128_c1.cu", "kern_n256_c1.cu", "kern_n256_c2.cu",
-                  "kern_n256_c2mc.cu", "kern_n256_c4mc.cu", "kern_n256_c2x2.cu"]
+# the device code of the GEMM kernel (the per-shape .cu files only instantiate it; launch
+# helpers are host code)
+KERNEL_SOURCES = ["kernel.cuh", "ptx.cuh"]
 
 
 def parse():
