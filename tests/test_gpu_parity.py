@@ -1,6 +1,5 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element,
 and the device ownership log against the coverage model (bit-exact invariants)."""
-import math
 
 import numpy as np
 import pytest

@@ -1,7 +1,6 @@
 """Programmatic dependent launch: a GEMM launched with `pdl` may start its prologue while
 the previous kernel on the stream still runs, but every access to global memory waits for
 that kernel.  Checked through the data the launches share."""
-import numpy as np
 import pytest
 import torch
 
