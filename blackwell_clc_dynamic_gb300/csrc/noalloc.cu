@@ -19,7 +19,8 @@
 //     Calls that overlap on the GPU (other streams, other threads) race on the array:
 //     serialise them.
 //   - the first call on a device (with that device current) looks up the array's
-//     device address with cudaGetSymbolAddress; make that first call before any stream
+//     device address with cudaGetSymbolAddress and launches every kernel once over an
+//     empty problem (waiting on a private stream); make that first call before any stream
 //     capture begins.
 //   - nothing here calls cudaMalloc, cudaFree or an allocating library routine.
 #include <cuda.h>

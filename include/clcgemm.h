@@ -278,8 +278,9 @@ CLCGEMM_API int gemm_occupy_stop(gemm_handle_t h, int *status);
  *     exits.  At most 65536 CTA tiles and 65536 launched workers per call; larger
  *     problems return GEMM_ERR_SCRATCH_LIMIT and launch nothing.
  *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
- *   - The first call on a device (that device current) resolves the array's address;
- *     make that first call before any stream capture begins.
+ *   - The first call on a device (that device current) resolves the array's address and
+ *     launches every kernel once over an empty problem on a private stream, waiting for
+ *     them (see gemm_create); make that first call before any stream capture begins.
  *   - All calls share the array: each clears what must start at zero on its own stream,
  *     but calls that overlap on the GPU (different streams or threads) race.  The log
  *     and error word it writes are not read back by any entry point; device-side wait
