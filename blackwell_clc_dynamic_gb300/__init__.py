@@ -6,7 +6,9 @@ module-level functions carry the C names (``gemm_create``, ``gemm_run``, ...); t
 call takes a device or host pointer; PyTorch supplies memory and streams, nothing else.
 
 Importing works without a GPU (the library loads and reports GEMM_ERR_NO_DEVICE on
-use); a missing library is an ImportError, never a silent fallback.
+use); a missing library is an ImportError, never a silent fallback.  With the
+environment variable CLCGEMM_CHECKED=1 the bounds-checked build (libclcgemm_checked.so,
+``build.py --checked``) is loaded instead.
 """
 from __future__ import annotations
 
@@ -15,7 +17,8 @@ import os
 from typing import Optional, Sequence, Tuple
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libclcgemm.so")
+CHECKED = os.environ.get("CLCGEMM_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "libclcgemm_checked.so" if CHECKED else "libclcgemm.so")
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = -1
@@ -28,6 +31,8 @@ GEMM_ERR_CUDA = -7
 GEMM_ERR_NO_DEVICE = -8
 GEMM_ERR_TOO_LARGE = -9
 GEMM_ERR_SCRATCH_LIMIT = -10
+GEMM_ERR_MULTICAST = -11
+GEMM_ERR_BOUNDS = -12
 
 GEMM_SCHED_CLC = 0
 GEMM_SCHED_STATIC = 1
@@ -40,6 +45,7 @@ EXPORTS = (
     "gemm_run_host", "gemm_sync", "gemm_device_error", "gemm_last_launch", "gemm_get_log", "gemm_get_trace",
     "gemm_max_active_clusters", "gemm_sm_count", "gemm_occupy_start", "gemm_occupy_wait_resident",
     "gemm_occupy_stop", "gemm_strerror", "gemm_version", "gemm_run_noalloc", "gemm_run_grouped_v",
+    "gemm_noalloc_status",
 )
 
 
@@ -55,7 +61,7 @@ class gemm_opts_t(ctypes.Structure):
     _fields_ = [("log_enable", ctypes.c_int), ("trace_enable", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
                 ("inject_fail_after", ctypes.c_int), ("raster_group", ctypes.c_int), ("l2_prefetch", ctypes.c_int),
                 ("hold_scheduler", ctypes.c_int), ("cluster_b_multicast", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("fetch_ahead", ctypes.c_int)]
+                ("fetch_ahead", ctypes.c_int), ("multicast", ctypes.c_int)]
 
 
 class gemm_launch_info_t(ctypes.Structure):
@@ -72,7 +78,8 @@ class GemmError(RuntimeError):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libclcgemm.so is not built ({LIB_PATH}); run blackwell_clc_dynamic_gb300/build.py")
+        raise ImportError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
+                          f"blackwell_clc_dynamic_gb300/build.py{' --checked' if CHECKED else ''}")
     lib = ctypes.CDLL(LIB_PATH)
     H = ctypes.c_void_p
     i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
@@ -101,6 +108,7 @@ def _load() -> ctypes.CDLL:
         "gemm_strerror": (ctypes.c_char_p, [i32]),
         "gemm_version": (i32, []),
         "gemm_run_noalloc": (i32, [i64, i64, i64, p, p, p, gemm_tile_t, gemm_cluster_t, i32, i32, p]),
+        "gemm_noalloc_status": (i32, [ctypes.POINTER(ctypes.c_int32), p, p, p, i64, i64, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -215,6 +223,19 @@ def gemm_run_noalloc(M, N, K, A, B, C, tile=(128, 256, 64), cluster=1, sched="cl
                                 num_workers, _stream(stream))
 
 
+def gemm_noalloc_status(n_tiles: int, n_workers: int, stream=None):
+    """(rc, (bits, site, block), owner, claims, first) of the latest gemm_run_noalloc call on
+    the current device: its device error word and ownership log (see the C header)."""
+    import numpy as np
+    w = (ctypes.c_int32 * 3)()
+    owner = np.empty(n_tiles, dtype=np.int32)
+    claims = np.empty(n_tiles, dtype=np.int32)
+    first = np.empty(n_workers, dtype=np.int32)
+    rc = lib.gemm_noalloc_status(w, owner.ctypes.data, claims.ctypes.data, first.ctypes.data, n_tiles, n_workers,
+                                 _stream(stream))
+    return rc, tuple(w), owner, claims, first
+
+
 def gemm_run_grouped_v(h, M_g: Sequence[int], N_g: Sequence[int], K_g: Sequence[int], A_g, B_g, C_g,
                        tile=(128, 256, 64), cluster=1, sched="clc", num_workers=0, stream=None) -> int:
     G = len(M_g)
@@ -239,10 +260,10 @@ class Gemm:
     def __init__(self, device: int = 0, log: bool = True, trace: bool = False, timeout_ns: int = 0,
                  inject_fail_after: int = -1, raster_group: int = 16, l2_prefetch: int = -1,
                  hold_scheduler: bool = False, cluster_b_multicast: bool = False, pdl: bool = False,
-                 fetch_ahead: int = 0):
+                 fetch_ahead: int = 0, multicast: bool = True):
         self.opts = gemm_opts_t(int(log), int(trace), int(timeout_ns), int(inject_fail_after), int(raster_group),
                                 int(l2_prefetch), int(hold_scheduler), int(cluster_b_multicast), int(pdl),
-                                int(fetch_ahead))
+                                int(fetch_ahead), int(multicast))
         rc, h = gemm_create(device, self.opts)
         _check(rc, "gemm_create")
         self.h = h

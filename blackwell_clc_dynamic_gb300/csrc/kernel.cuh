@@ -40,8 +40,17 @@ constexpr int TRACE_WORDS = 8;   // u64 per CTA tile in the optional trace
 // higher (square 8192^3: +3-8 %; pair, grouped and tail shapes equal or slightly faster).
 constexpr int kDefaultRasterGroup = 16;
 
-// Device error word: [0] bits, [1] first failing wait site, [2] block of that wait.
-enum : int { ERRB_TIMEOUT = 1 };
+// Device error word: [0] bits, [1] first failing wait site (or 100 + failed bounds check),
+// [2] block of that failure.
+enum : int { ERRB_TIMEOUT = 1, ERRB_BOUNDS = 2 };
+// Bounds checks of the checked build (compiled with CLCG_BOUNDS_CHECK): which invariant of
+// a work tile failed.
+#ifdef CLCG_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+enum : int { CHK_GROUP = 101, CHK_ROW = 102, CHK_COL = 103, CHK_POS = 104, CHK_WORKER = 105, CHK_KB = 106 };
 enum : int {
   WAIT_EMPTY = 1, WAIT_FULL = 2, WAIT_ACC_EMPTY = 3, WAIT_ACC_FULL = 4, WAIT_CLC_FULL = 5,
   WAIT_CLC_EMPTY = 6, WAIT_THR_FULL = 7, WAIT_THR_EMPTY = 8
@@ -77,6 +86,8 @@ struct Params {
   int hold_scheduler;            // test hook: the CLC scheduler issues and signals nothing
   int pdl;                       // launched as a programmatic dependent of the previous kernel
   int fetch_ahead;               // extra throttle tokens: the scheduler fetches this many more tiles ahead
+  long long n_tiles;             // CTA tiles of the launch (ownership-log entries); checked build only
+  long long n_workers;           // launched workers (first-tile entries); checked build only
 };
 
 // Cluster shapes:
@@ -213,7 +224,17 @@ struct Work {
   int pos;     // ownership-log index of this CTA's tile
   int kb;      // k-blocks of this tile's problem
   bool valid;
+  bool skip;   // checked build: a bounds check failed; every role passes over the tile
 };
+
+// Checked build: record a failed bounds check in the error word (first failure's site and
+// block), never trap.
+__device__ __forceinline__ void report_bounds(const Params& p, int site) {
+  if ((atomicOr(p.err, ERRB_BOUNDS) & (ERRB_TIMEOUT | ERRB_BOUNDS)) == 0) {
+    p.err[1] = site;
+    p.err[2] = (int)blockIdx.x;
+  }
+}
 
 // Raster / swizzle: bands of `group` tile rows; inside a band the row index runs fastest.
 __device__ __forceinline__ void raster_map(int c, int mt, int nt, int group, int& m, int& n) {
@@ -234,6 +255,7 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
   w.n_blk = 0;
   w.pos = 0;
   w.kb = 0;
+  w.skip = false;
   if (!w.valid) return w;
   int base = 0, mt = p.mt, nt = p.nt, kb = p.k_blocks, g = 0;
   if (p.G > 0) {
@@ -257,6 +279,21 @@ __device__ __forceinline__ Work make_work(const Params& p, int c, uint32_t rank)
   w.n_blk = n * RN + (int)rank % RN;
   w.pos = base * CL + w.m_blk * (nt * RN) + w.n_blk;
   w.kb = kb;
+  if constexpr (kBoundsCheck) {
+    // Every index the roles derive from the tile: its problem, its row and column block
+    // inside the problem's cluster-tile grid, its log entry, its k-loop length.  A failure
+    // is recorded and every role passes over the tile (all roles derive the same Work).
+    int site = 0;
+    if (p.G > 0 && (g < 0 || g >= p.G)) site = CHK_GROUP;
+    else if (w.m_blk < 0 || w.m_blk >= mt * (CL / RN)) site = CHK_ROW;
+    else if (w.n_blk < 0 || w.n_blk >= nt * RN) site = CHK_COL;
+    else if (w.pos < 0 || (long long)w.pos >= p.n_tiles) site = CHK_POS;
+    else if (kb < 0) site = CHK_KB;
+    if (site) {
+      report_bounds(p, site);
+      w.skip = true;
+    }
+  }
   return w;
 }
 
@@ -449,6 +486,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (SCHED == SCHED_CLC && rank == 0) {
           if (!produce_token(tile + ahead)) break;
         }
+        if (kBoundsCheck && w.skip) {   // checked build: a tile that failed a bounds check
+          ++tile;
+          w = it.next(p, rank, sb, ctl, false);
+          continue;
+        }
         if (p.trace) p.trace[TRACE_WORDS * (size_t)w.pos + 0] = globaltimer();
         const CUtensorMap* mA = p.G ? p.gmaps + 3 * w.g : &p.tmA;
         const CUtensorMap* mB = p.G ? p.gmaps + 3 * w.g + 1 : &p.tmB;
@@ -497,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         ++tile;
         const uint64_t t_req = p.trace ? globaltimer() : 0;
         w = it.next(p, rank, sb, ctl, false);
-        if (p.trace && w.valid) p.trace[TRACE_WORDS * (size_t)w.pos + 4] = globaltimer() - t_req;
+        if (p.trace && w.valid && !w.skip) p.trace[TRACE_WORDS * (size_t)w.pos + 4] = globaltimer() - t_req;
       }
     }
     __syncwarp();
@@ -513,6 +555,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       constexpr uint32_t idesc = make_idesc<C::MMA_M, BN>();
       constexpr uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
       while (w.valid) {
+        if (kBoundsCheck && w.skip) {
+          w = it.next(p, rank, sb, ctl, false);
+          continue;
+        }
         if (!bar_wait<PAIR>(bar(C::BAR_ACC_EMPTY + acc), aph ^ 1, p, ctl, WAIT_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -587,7 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           fence_proxy_async_smem();
           if (ok && p.trace) {
             const Work got = make_work<CL, RN>(p, (int)(x / C::CLX), 0);
-            if (got.valid) p.trace[TRACE_WORDS * (size_t)got.pos + 5] = globaltimer() - t_issue;
+            if (got.valid && !got.skip) p.trace[TRACE_WORDS * (size_t)got.pos + 5] = globaltimer() - t_issue;
           }
         }
         mbar_arrive(bar(C::BAR_CLC_EMPTY + s));
@@ -608,6 +654,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const uint32_t acc_empty_leader0 = PAIR ? map_to_rank(bar(C::BAR_ACC_EMPTY), 0) : bar(C::BAR_ACC_EMPTY);
     int chunk_seq = 0;
     while (w.valid) {
+      if (kBoundsCheck && w.skip) {
+        w = it.next(p, rank, sb, ctl, true);
+        continue;
+      }
       if (!bar_wait(bar(C::BAR_ACC_FULL + acc), aph, p, ctl, WAIT_ACC_FULL)) break;
       tc_fence_after();
       if (p.trace && q == 0 && lane == 0) p.trace[TRACE_WORDS * (size_t)w.pos + 6] = globaltimer();
@@ -659,8 +709,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         if (p.log_owner) {
           p.log_owner[w.pos] = worker;
           log_claim(p.log_claims + w.pos, p.log_epoch);
-          if (first_tile && rank == 0)
-            p.log_first[worker] = ((unsigned long long)p.log_epoch << 32) | (unsigned)w.c;
+          if (first_tile && rank == 0) {
+            if (kBoundsCheck && (worker < 0 || (long long)worker >= p.n_workers)) report_bounds(p, CHK_WORKER);
+            else p.log_first[worker] = ((unsigned long long)p.log_epoch << 32) | (unsigned)w.c;
+          }
         }
         if (p.trace) {
           p.trace[TRACE_WORDS * (size_t)w.pos + 1] = globaltimer();

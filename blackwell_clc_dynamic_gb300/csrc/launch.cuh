@@ -97,9 +97,28 @@ cudaError_t warm_n256_c2mc(const Params& p0, cudaStream_t s);
 cudaError_t warm_n256_c4mc(const Params& p0, cudaStream_t s);
 cudaError_t warm_n256_c2x2(const Params& p0, cudaStream_t s);
 
+// Shapes whose CTAs share operand tiles by TMA multicast loads: clusters of 2 that run
+// their own MMAs (not the CTA pair), clusters of 4 (4 x 1 x 1 and 2 x 2 x 1).  They run only
+// in a process that sees one GPU, on memory of that GPU.
+inline bool uses_tma_multicast(int cl, bool pair) { return cl == 4 || (cl == 2 && !pair); }
+
+// True when `p` points into device memory of device `dev`: not host (pinned or pageable),
+// not managed, not another GPU's memory.  Every tensor map is encoded only over such
+// memory.
+inline bool on_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  memset(&a, 0, sizeof a);
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
 // Launch every kernel of the library once over an empty problem on stream `s` (see
-// warm_shape) and wait for them.  `err` receives device error words (none are expected).
-inline cudaError_t warm_all(int* err, cudaStream_t s) {
+// warm_shape) and wait for them; the TMA multicast shapes only if `with_multicast`.
+// `err` receives device error words (none are expected).
+inline cudaError_t warm_all(int* err, cudaStream_t s, bool with_multicast) {
   Params p0;
   memset(&p0, 0, sizeof p0);
   p0.total = 0;               // no tile: every role exits at once
@@ -108,11 +127,17 @@ inline cudaError_t warm_all(int* err, cudaStream_t s) {
   p0.err = err;
   p0.timeout_ns = 2000000000LL;
   p0.inject_fail_after = -1;
-  cudaError_t (*fs[])(const Params&, cudaStream_t) = {warm_n128_c1, warm_n256_c1, warm_n256_c2, warm_n256_c2mc,
-                                                       warm_n256_c4mc, warm_n256_c2x2};
-  for (auto f : fs) {
+  cudaError_t (*plain[])(const Params&, cudaStream_t) = {warm_n128_c1, warm_n256_c1, warm_n256_c2};
+  cudaError_t (*mcast[])(const Params&, cudaStream_t) = {warm_n256_c2mc, warm_n256_c4mc, warm_n256_c2x2};
+  for (auto f : plain) {
     cudaError_t e = f(p0, s);
     if (e != cudaSuccess) return e;
+  }
+  if (with_multicast) {
+    for (auto f : mcast) {
+      cudaError_t e = f(p0, s);
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaStreamSynchronize(s);
 }

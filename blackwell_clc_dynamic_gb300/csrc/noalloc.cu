@@ -22,7 +22,11 @@
 //     device address with cudaGetSymbolAddress and launches every kernel once over an
 //     empty problem (waiting on a private stream); make that first call before any stream
 //     capture begins.
-//   - nothing here calls cudaMalloc, cudaFree or an allocating library routine.
+//   - nothing here calls cudaMalloc, cudaFree or an allocating library routine;
+//   - gemm_noalloc_status copies the error word and the log of the latest call back to
+//     the caller (a wait that ran out leaves C incomplete; that call reports it);
+//   - the shapes whose CTAs share operand tiles by TMA multicast run only when the
+//     process sees one GPU, and A, B, C must be memory of the current device.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -51,7 +55,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t* g_scratch_dev[kMaxDevices];   // device address of g_noalloc_scratch, per device
 int g_sms[kMaxDevices];
+bool g_single_gpu[kMaxDevices];        // the process sees one GPU: multicast shapes allowed
 uint32_t g_epoch[kMaxDevices];         // log tag of the device's most recent call
+int64_t g_last_tiles[kMaxDevices];     // CTA tiles and launched workers of that call (-1: none yet)
+int64_t g_last_workers[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int from_cuda(cudaError_t e) {
@@ -79,19 +86,26 @@ int setup_device(int dev) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return from_cuda(e);
   if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  int n_dev = 0;
+  e = cudaGetDeviceCount(&n_dev);
+  if (e != cudaSuccess) return from_cuda(e);
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess || p == nullptr) return from_cuda(e == cudaSuccess ? cudaErrorUnknown : e);
-  // launch every kernel once over an empty problem now, rather than have a first launch
-  // load code later (see warm_all); the error words of the scratch take any report
+  // launch every kernel this device may run once over an empty problem now, rather than
+  // have a first launch load code later (see warm_all); the error words of the scratch
+  // take any report
   cudaStream_t st = nullptr;
   e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
   if (e != cudaSuccess) return from_cuda(e);
-  e = warm_all(static_cast<int32_t*>(p), st);
+  e = warm_all(static_cast<int32_t*>(p), st, n_dev == 1);
   cudaStreamDestroy(st);
   if (e != cudaSuccess) return from_cuda(e);
   g_scratch_dev[dev] = static_cast<int32_t*>(p);
   g_sms[dev] = sms;
+  g_single_gpu[dev] = n_dev == 1;
+  g_last_tiles[dev] = -1;
+  g_last_workers[dev] = -1;
   return GEMM_OK;
 }
 
@@ -146,6 +160,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   if (e != cudaSuccess) return from_cuda(e);
   int rc = setup_device(dev);
   if (rc) return rc;
+  if (uses_tma_multicast(cl, pair) && !g_single_gpu[dev]) return GEMM_ERR_MULTICAST;
+  if (!on_device(C, dev) || (K > 0 && (!on_device(A, dev) || !on_device(B, dev)))) return GEMM_ERR_INVALID_ARG;
 
   const int64_t tile_m = (int64_t)BM * (cl / rn), tile_n = (int64_t)bn * rn;   // cluster tile
   const int64_t mt = (M + tile_m - 1) / tile_m;
@@ -169,6 +185,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     epoch = g_epoch[dev] + 1;
     if (epoch >= (1u << 24)) epoch = 1;
     g_epoch[dev] = epoch;
+    g_last_tiles[dev] = n_tiles;
+    g_last_workers[dev] = workers;
   }
   e = cudaMemsetAsync(err, 0, kErrWords * sizeof(int32_t), s);
   if (e == cudaSuccess && epoch == 1) {
@@ -205,6 +223,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
   p.err = err;
   p.timeout_ns = 2000000000LL;
   p.inject_fail_after = -1;
+  p.n_tiles = n_tiles;
+  p.n_workers = workers;
 
   const int grid = (int)(workers * cl);
   e = launch_any(bn, cl, pair, (int)sched, p, grid, s, rn);
@@ -212,5 +232,68 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, 
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;
   }
+  return GEMM_OK;
+}
+
+extern "C" int gemm_noalloc_status(int32_t out3[3], int32_t* owner, int32_t* claims, int32_t* first, int64_t n_tiles,
+                                   int64_t n_workers, void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_INVALID_ARG;
+  int32_t* err;
+  uint32_t epoch;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    err = g_scratch_dev[dev];
+    if (!err || g_last_tiles[dev] < 0) return GEMM_ERR_INVALID_ARG;   // no call on this device yet
+    if ((owner || claims || first) && (n_tiles != g_last_tiles[dev] || n_workers != g_last_workers[dev]))
+      return GEMM_ERR_INVALID_ARG;
+    epoch = g_epoch[dev];
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every copy is ordered after the call on its stream and waited for at once
+  auto copy = [&](void* dst, const void* src, size_t bytes) -> cudaError_t {
+    cudaError_t x = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s);
+    return x == cudaSuccess ? cudaStreamSynchronize(s) : x;
+  };
+  int32_t w[3] = {0, 0, 0};
+  e = copy(w, err, sizeof w);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (out3) memcpy(out3, w, sizeof w);
+  const int32_t* d_owner = err + kErrWords;
+  const uint32_t* d_claims = reinterpret_cast<const uint32_t*>(d_owner + kNoAllocMaxTiles);
+  const unsigned long long* d_first = reinterpret_cast<const unsigned long long*>(d_claims + kNoAllocMaxTiles);
+  // Copied in chunks through small buffers on the stack: entries carry the tag of the
+  // call that wrote them, and only the latest call's count as written.
+  constexpr int64_t kChunk = 1024;
+  uint32_t raw_c[kChunk];
+  unsigned long long raw_f[kChunk];
+  if (owner && n_tiles > 0) {
+    e = copy(owner, d_owner, (size_t)n_tiles * 4);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (owner || claims) {
+    for (int64_t t0 = 0; t0 < n_tiles; t0 += kChunk) {
+      const int64_t n = n_tiles - t0 < kChunk ? n_tiles - t0 : kChunk;
+      e = copy(raw_c, d_claims + t0, (size_t)n * 4);
+      if (e != cudaSuccess) return from_cuda(e);
+      for (int64_t i = 0; i < n; ++i) {
+        const int32_t cnt = (raw_c[i] >> 8) == epoch ? (int32_t)(raw_c[i] & 0xFFu) : 0;
+        if (claims) claims[t0 + i] = cnt;
+        if (owner && cnt == 0) owner[t0 + i] = -1;
+      }
+    }
+  }
+  if (first) {
+    for (int64_t w0 = 0; w0 < n_workers; w0 += kChunk) {
+      const int64_t n = n_workers - w0 < kChunk ? n_workers - w0 : kChunk;
+      e = copy(raw_f, d_first + w0, (size_t)n * 8);
+      if (e != cudaSuccess) return from_cuda(e);
+      for (int64_t i = 0; i < n; ++i)
+        first[w0 + i] = (uint32_t)(raw_f[i] >> 32) == epoch ? (int32_t)(uint32_t)raw_f[i] : -1;
+    }
+  }
+  if (w[0] != 0) return (w[0] & ERRB_TIMEOUT) ? GEMM_ERR_TIMEOUT : GEMM_ERR_BOUNDS;
   return GEMM_OK;
 }

@@ -53,7 +53,8 @@ def test_strerror_and_version(pkg):
 def test_opts_default(pkg):
     o = pkg.gemm_opts_default()
     assert (o.log_enable, o.trace_enable, o.timeout_ns, o.inject_fail_after, o.raster_group, o.l2_prefetch,
-            o.hold_scheduler, o.cluster_b_multicast, o.pdl, o.fetch_ahead) == (1, 0, 2_000_000_000, -1, 16, 0, 0, 0, 0, 0)
+            o.hold_scheduler, o.cluster_b_multicast, o.pdl, o.fetch_ahead,
+            o.multicast) == (1, 0, 2_000_000_000, -1, 16, 0, 0, 0, 0, 0, 1)
 
 
 def test_create_without_gpu_reports_no_device(pkg):
@@ -62,6 +63,28 @@ def test_create_without_gpu_reports_no_device(pkg):
         pytest.skip("a GPU is present")
     rc, h = pkg.gemm_create(0)
     assert rc == pkg.GEMM_ERR_NO_DEVICE and h is None
+
+
+def test_checked_build_exports_the_same_symbols(pkg):
+    """The bounds-checked build (CLCG_BOUNDS_CHECK) is the same library with checks added."""
+    import __graft_entry__
+    path = __graft_entry__._load_build_module().build(checked=True)
+    lib = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_new_error_codes_are_named(pkg):
+    assert "multicast" in pkg.gemm_strerror(pkg.GEMM_ERR_MULTICAST)
+    assert "bounds" in pkg.gemm_strerror(pkg.GEMM_ERR_BOUNDS)
+
+
+def test_noalloc_status_without_device(pkg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, words, owner, claims, first = pkg.gemm_noalloc_status(0, 0)
+    assert rc == pkg.GEMM_ERR_NO_DEVICE
 
 
 def test_null_handle_is_rejected(pkg):

@@ -1,4 +1,5 @@
 """Pins for the tile-coverage model and the raster map (no GPU)."""
+import itertools
 import json
 import math
 import os
@@ -71,14 +72,90 @@ def test_static_planned_above_resident_tail():
     assert clc.makespan == math.ceil(4096 / 62)
 
 
-@pytest.mark.parametrize("T,R", [(1, 1), (3, 2), (5, 2), (6, 3), (7, 3), (7, 2)])
-@pytest.mark.parametrize("prefetch", [False, True])
-def test_exhaustive_cancel_orders_keep_coverage(T, R, prefetch):
-    n = 0
-    for s in cv.enumerate_clc_orders(T, R, prefetch=prefetch):
+def _check_every_order_once(schedules, T, R):
+    """With the plain fetch (a worker cancels when its tile ends) the R first launches start
+    at once and each later launch is obtained by exactly one successful cancel, one at a
+    time, each choosing freely among the launches still pending ("CUTLASS CLC dynamic
+    persistent kernel", section "What is cancelled is a launch, what is obtained is a work
+    coordinate": only atomicity is fixed).  The orders in which launches R .. T-1 are
+    cancelled are therefore exactly the permutations of those ids, (T - R)! of them, and an
+    exhaustive enumeration must produce each once."""
+    seqs = [tuple(s.cancelled) for s in schedules]
+    expected = set(itertools.permutations(range(R, T)))
+    assert len(seqs) == math.factorial(max(T - R, 0)), "number of cancel orders"
+    assert len(set(seqs)) == len(seqs), "an order was enumerated twice"
+    assert set(seqs) == expected, "the enumerated orders are not the permutations of the pending launches"
+
+
+@pytest.mark.parametrize("T,R", [(1, 1), (2, 1), (4, 1), (6, 1), (3, 2), (5, 2), (6, 3), (7, 3), (7, 2), (2, 5)])
+def test_cancel_orders_are_all_permutations_once(T, R):
+    scheds = list(cv.enumerate_clc_orders(T, R))
+    for s in scheds:
         cv.check_schedule(s)
-        n += 1
-    assert n >= 1
+    _check_every_order_once(scheds, T, R)
+    if R == 1:
+        # one resident worker: launch 0 runs its own tile, then the cancelled ones in order
+        for s in scheds:
+            assert s.sequences == {0: [0] + list(s.cancelled)}
+            assert s.makespan == T
+
+
+def test_truncated_or_repeating_enumerations_are_caught():
+    """Planted mistakes in an enumerator: stopping after the first branch, or yielding a
+    schedule twice, must fail the check above."""
+    T, R = 5, 2
+    with pytest.raises(AssertionError):
+        _check_every_order_once(itertools.islice(cv.enumerate_clc_orders(T, R), 1), T, R)
+    scheds = list(cv.enumerate_clc_orders(T, R))
+    with pytest.raises(AssertionError):
+        _check_every_order_once(scheds[:-1] + scheds[:1], T, R)
+    with pytest.raises(AssertionError):
+        _check_every_order_once(scheds[:-1], T, R)
+
+
+def _brute_force_choice_sequences(T, R, prefetch, cost):
+    """Every sequence of choices the model can make, found without the enumerator's search:
+    run the model once for every tuple of T choice indices (index i picks the i-th smallest
+    pending launch) and keep the tuples whose every used index was valid; the used prefix
+    of such a tuple is one distinct schedule."""
+    found = set()
+    for idx in itertools.product(range(max(T, 1)), repeat=T):
+        used = []
+        bad = []
+
+        def pick(pending):
+            k = idx[len(used)]
+            used.append(k)
+            if k >= len(pending):
+                bad.append(k)
+                return sorted(pending)[0]
+            return sorted(pending)[k]
+
+        cv.simulate(T, cv.CLC, R, cost=cost, pick=pick, prefetch=prefetch)
+        if not bad:
+            found.add(tuple(used))
+    return found
+
+
+@pytest.mark.parametrize("T,R", [(1, 1), (3, 1), (3, 2), (4, 2), (5, 2), (5, 3)])
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_enumeration_matches_brute_force(T, R, prefetch):
+    """The enumerator's schedules are exactly the model's reachable choice sequences, each
+    once (also with the overlapped fetch, where no closed form counts them)."""
+    rng = random.Random(T * 10 + R)
+    cost = [rng.choice([0.5, 1.0, 2.0]) for _ in range(T)]
+    got = []
+    for s in cv.enumerate_clc_orders(T, R, prefetch=prefetch, cost=cost):
+        cv.check_schedule(s)
+        got.append(tuple(s.cancelled))
+    # map each brute-force choice sequence to its cancelled-launch sequence
+    expected = set()
+    for choices in _brute_force_choice_sequences(T, R, prefetch, cost):
+        it = iter(choices)
+        s = cv.simulate(T, cv.CLC, R, cost=cost, pick=lambda p: sorted(p)[next(it)], prefetch=prefetch)
+        expected.add(tuple(s.cancelled))
+    assert len(got) == len(set(got)) == len(expected)
+    assert set(got) == expected
 
 
 def test_exhaustive_with_uneven_costs():

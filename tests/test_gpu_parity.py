@@ -129,6 +129,47 @@ def test_argument_errors(g):
     assert m.gemm_run(h, 128, 256, 64, None, B, C) == m.GEMM_ERR_INVALID_ARG
 
 
+def test_operands_must_be_memory_of_the_handles_device(g):
+    """A, B and C must be device memory of the handle's GPU: pinned host memory (which the
+    GPU could reach) is refused before any tensor map is encoded, for every entry point."""
+    import blackwell_clc_dynamic_gb300 as m
+    A = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((128, 256), dtype=torch.float32, device="cuda")
+    Ah, Bh, Ch = A.cpu().pin_memory(), B.cpu().pin_memory(), C.cpu().pin_memory()
+    h = g.h
+    for args in ((Ah, B, C), (A, Bh, C), (A, B, Ch)):
+        assert m.gemm_run(h, 128, 256, 64, *args) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run_grouped(h, [128], 256, 64, [Ah], [B], [C]) == m.GEMM_ERR_INVALID_ARG
+    assert m.gemm_run_grouped_v(h, [128], [256], [64], [A], [B], [Ch]) == m.GEMM_ERR_INVALID_ARG
+    # the same operands in device memory run
+    assert m.gemm_run(h, 128, 256, 64, A, B, C) == m.GEMM_OK
+    assert m.gemm_run_grouped(h, [128], 256, 64, [A], [B], [C]) == m.GEMM_OK
+    g.sync()
+
+
+def test_handle_without_multicast_refuses_the_multicast_shapes():
+    """A handle created with multicast = 0 (what every process of a multi-GPU job uses)
+    never launches a kernel whose CTAs share operand tiles by TMA multicast; the CTA pair
+    and one-CTA shapes still run."""
+    import blackwell_clc_dynamic_gb300 as m
+    A = wl.make_matrix((512, 256), 301, "int")
+    B = wl.make_matrix((256, 512), 302, "int")
+    with m.Gemm(0, multicast=False) as h:
+        dA, dB = A.cuda(), B.cuda()
+        C = torch.zeros((512, 512), dtype=torch.float32, device="cuda")
+        for cl in (4, (2, 2, 1)):
+            assert m.gemm_run(h.h, 512, 512, 256, dA, dB, C, cluster=cl) == m.GEMM_ERR_MULTICAST
+        h.set_opts(cluster_b_multicast=1, multicast=1)      # multicast stays as created
+        assert m.gemm_run(h.h, 512, 512, 256, dA, dB, C, cluster=2) == m.GEMM_ERR_MULTICAST
+        with pytest.raises(m.GemmError):
+            h.max_active_clusters(TILE_256, 4)
+        h.set_opts(cluster_b_multicast=0)
+        ref = oracle.gemm(A, B)
+        for cl in (1, 2):
+            assert np.array_equal(run(h, A, B, cluster=cl).astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("T", [1, 2, 5])
 def test_static_owner_map_exact(g, T):
     """Static: tile t is run by worker t mod W, bit-exact; W above the tile count too."""
@@ -192,27 +233,18 @@ def test_clc_injected_failure_keeps_coverage(g, n_fetch):
 
 
 @pytest.mark.parametrize("T", [147, 148, 149, 296, 297])
-def test_tail_sweep_sampled(g, T):
-    """Tail sweep workload (M = 128 T, N = 256, K = 8192, seed 2), CLC and static-persistent:
-    the first and last tile in full plus 512 scattered elements against the oracle."""
+def test_tail_sweep_full(g, T):
+    """Tail sweep workload (M = 128 T, N = 256, K = 8192, seed 2), CLC, static-persistent
+    (148 workers) and non-persistent: every element of C against the oracle."""
     w = wl.tail(T)
     A, B = wl.make_inputs(w)
     dA, dB = A.cuda(), B.cuda()
-    rng = np.random.default_rng(T)
-    rows = rng.integers(0, w.M, 512)
-    cols = rng.integers(0, w.N, 512)
-    ref_e = oracle.gemm_entries(A, B, rows, cols)
-    ref_first = oracle.gemm_block(A, B, 0, 128, 0, 256)
-    ref_last = oracle.gemm_block(A, B, w.M - 128, w.M, 0, 256)
-    for mode in ("clc", "static"):
+    ref = oracle.gemm(A, B)
+    for mode in MODES:
         C = torch.full((w.M, w.N), float("nan"), device="cuda")
         g.run(dA, dB, C, sched=mode, num_workers=148)
         g.sync()
-        Ch = C.cpu().numpy()
-        assert_close(Ch[rows, cols], ref_e)
-        assert_close(Ch[:128], ref_first)
-        assert_close(Ch[-128:], ref_last)
-        assert not np.isnan(Ch).any()
+        assert_close(C.cpu().numpy(), ref)
         check_log(g, mode, [T], 1, 1, num_workers=148 if mode == "static" else None)
 
 
@@ -250,43 +282,114 @@ def test_run_host_matches_device_run(g):
 
 
 _INPUTS = {}
+_REFS = {}
 
 
 def _inputs(w):
-    """Seeded inputs of a full-size workload, drawn once per test session."""
+    """Seeded inputs of a full-size workload, drawn once per test session (one workload
+    held at a time)."""
     if w.name not in _INPUTS:
         _INPUTS.clear()
+        _REFS.clear()
         _INPUTS[w.name] = wl.make_inputs(w)
     return _INPUTS[w.name]
 
 
-def _sampled_check(A, B, C_dev, M, N, rng, n_entries=512, blocks=()):
-    Ch = C_dev.cpu().numpy()
-    assert not np.isnan(Ch).any(), "an output element was never written"
-    rows = rng.integers(0, M, n_entries)
-    cols = rng.integers(0, N, n_entries)
-    assert_close(Ch[rows, cols], oracle.gemm_entries(A, B, rows, cols))
-    for r0, r1, c0, c1 in blocks:
-        assert_close(Ch[r0:r1, c0:c1], oracle.gemm_block(A, B, r0, r1, c0, c1))
+def _reference(w):
+    """The oracle's C of a full-size workload (every element, fp64; a list of per-problem
+    results for grouped workloads), computed once and shared by the schedules compared
+    with it."""
+    A, B = _inputs(w)
+    if w.name not in _REFS:
+        _REFS[w.name] = [oracle.gemm(a, b) for a, b in zip(A, B)] if w.group_m else oracle.gemm(A, B)
+    return _REFS[w.name]
+
+
+def _full_check(C_dev, ref):
+    """Every element of C against the oracle at the stated tolerance; an element the kernel
+    never wrote stays NaN and fails."""
+    assert_close(C_dev.cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_square_full_size_sampled(g, mode):
-    """M = N = K = 8192 (seed 1), 128 x 256 tiles, the bench's launch configuration."""
+def test_square_full_size(g, mode):
+    """M = N = K = 8192 (seed 1), 128 x 256 tiles, the bench's launch configuration: all of C
+    against the oracle."""
     w = wl.SQUARE
     A, B = _inputs(w)
+    ref = _reference(w)
     C = torch.full((w.M, w.N), float("nan"), device="cuda")
     g.run(A.cuda(), B.cuda(), C, sched=mode, num_workers=148)
     g.sync()
-    _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(2),
-                   blocks=[(0, 128, 0, 256), (w.M - 128, w.M, w.N - 256, w.N), (4096, 4224, 2048, 2304)])
+    _full_check(C, ref)
     check_log(g, mode, [64], 32, 1, num_workers=148 if mode == "static" else None)
+
+
+@pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0), (C2X2, 0)],
+                         ids=["pair", "c2_shared_b", "c4_shared_b", "c2x2_shared_ab"])
+def test_square_full_size_cluster_modes(g, cl, mcast):
+    """The square workload in the cluster launch configurations the benchmark times beside
+    the headline (CLC): all of C against the oracle, exact log."""
+    w = wl.SQUARE
+    A, B = _inputs(w)
+    ref = _reference(w)
+    mt, nt, ncta, rn = grid_of(w.M, w.N, TILE_256, cl)
+    g.set_opts(cluster_b_multicast=mcast)
+    try:
+        C = torch.full((w.M, w.N), float("nan"), device="cuda")
+        g.run(A.cuda(), B.cuda(), C, cluster=cl, sched="clc")
+        g.sync()
+        _full_check(C, ref)
+        check_log(g, "clc", [mt], nt, ncta, rn=rn)
+    finally:
+        g.set_opts(cluster_b_multicast=0)
+
+
+@pytest.mark.parametrize("shape", ["square", "tail297", "pair"])
+def test_clc_workers_steal(g, shape):
+    """On an otherwise idle GPU with many more tiles than resident workers, CLC really takes
+    work over ("CUTLASS CLC dynamic persistent kernel", section "What is cancelled is a
+    launch, what is obtained is a work coordinate"): no more workers run than can be
+    resident at once, workers run several tiles each, and the scheduler's trace names a
+    successful try_cancel round trip for exactly the tiles that were not their own
+    launch's, one per tile that no launch of its own computed (tiles - workers that ran)."""
+    w = {"square": wl.SQUARE, "tail297": wl.tail(297), "pair": wl.PAIR}[shape]
+    cl = 2 if shape == "pair" else 1
+    A, B = _inputs(w) if shape == "square" else wl.make_inputs(w)
+    mt, nt, ncta, rn = grid_of(w.M, w.N, TILE_256, cl)
+    resident = g.max_active_clusters(TILE_256, cl)
+    assert mt * nt > 2 * resident
+    g.set_opts(trace_enable=1)
+    try:
+        C = torch.full((w.M, w.N), float("nan"), device="cuda")
+        g.run(A.cuda(), B.cuda(), C, cluster=cl, sched="clc")
+        g.sync()
+        tr = g.get_trace().astype(np.int64)
+    finally:
+        g.set_opts(trace_enable=0)
+    assert not torch.isnan(C).any()
+    owner_lin, first = check_log(g, "clc", [mt], nt, ncta)
+    T = mt * nt
+    ran = sorted(set(owner_lin))
+    counts = np.bincount(np.array(owner_lin), minlength=T)
+    assert len(ran) <= resident, (len(ran), resident)
+    assert counts.max() > 1 and counts[ran].min() >= 1
+    stolen = np.array([owner_lin[t] != t for t in range(T)])
+    assert stolen.sum() == T - len(ran)
+    # round trips are recorded by rank 0's scheduler, on the CTA tile of rank 0 (cluster
+    # tiles are row-major over CTA rows; rank r holds row block m * ncta + r)
+    rt = np.zeros(T, dtype=np.int64)
+    for c in range(T):
+        m, n = cv.raster(c, mt, nt, g.opts.raster_group)
+        rt[c] = tr[(m * ncta) * nt + n, 5]
+    assert np.all(rt[stolen] > 0) and np.all(rt[~stolen] == 0)
 
 
 @pytest.mark.parametrize("mode", MODES)
 def test_pair_full_size_with_occupied_sms(g, mode):
     """M = N = 16384, K = 4096, normal(0, 0.02) (seed 3), 256 x 256 cluster tiles on CTA
-    pairs, while an occupier kernel on another stream holds 24 SMs for the whole run."""
+    pairs, while an occupier kernel on another stream holds 24 SMs for the whole run: all
+    of C against the oracle."""
     w = wl.PAIR
     A, B = _inputs(w)
     dA, dB = A.cuda(), B.cuda()
@@ -309,16 +412,14 @@ def test_pair_full_size_with_occupied_sms(g, mode):
     torch.cuda.synchronize()
     assert timed_out == 0
     g.sync()
-    _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(3),
-                   blocks=[(0, 256, 0, 256), (w.M - 256, w.M, w.N - 256, w.N)])
+    _full_check(C, _reference(w))
     check_log(g, mode, [64], 64, 2, num_workers=74 if mode == "static" else None)
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_grouped_full_size_sampled(g, mode):
+def test_grouped_full_size(g, mode):
     """64 problems, N = K = 4096, M_g = 128 ceil(lognormal(2, 1)) clipped to [128, 8192]
-    (seed 4), one flat grid of 12096 tiles of 128 x 256: first and last tile of every
-    problem plus scattered elements."""
+    (seed 4), one flat grid of 12096 tiles of 128 x 256: every C_g in full."""
     w = wl.grouped()
     As, Bs = _inputs(w)
     dA = [a.cuda() for a in As]
@@ -326,10 +427,8 @@ def test_grouped_full_size_sampled(g, mode):
     dC = [torch.full((m, w.N), float("nan"), device="cuda") for m in w.group_m]
     g.run_grouped(dA, dB, dC, sched=mode, num_workers=148)
     g.sync()
-    rng = np.random.default_rng(4)
-    for a, b, c, m in zip(As, Bs, dC, w.group_m):
-        _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
-                       blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
+    for c, ref in zip(dC, _reference(w)):
+        _full_check(c, ref)
     check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
 
 
@@ -372,9 +471,10 @@ def test_grouped_varied_shapes_small(g, tile, cl, mc, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_grouped_varied_depth_full_size_sampled(g, mode):
+def test_grouped_varied_depth_full_size(g, mode):
     """64 problems with K_g = 256 ceil(lognormal(2, 1)) in [256, 16384] and M_g as in the
-    grouped workload (seed 5), N = 4096: tiles of unequal cost in one flat grid."""
+    grouped workload (seed 5), N = 4096: tiles of unequal cost in one flat grid; every C_g
+    in full."""
     w = wl.grouped_varied_depth()
     As, Bs = _inputs(w)
     dA = [a.cuda() for a in As]
@@ -382,10 +482,8 @@ def test_grouped_varied_depth_full_size_sampled(g, mode):
     dC = [torch.full((m, w.N), float("nan"), device="cuda") for m in w.group_m]
     g.run_grouped_v(dA, dB, dC, sched=mode, num_workers=148)
     g.sync()
-    rng = np.random.default_rng(5)
-    for a, b, c, m in zip(As, Bs, dC, w.group_m):
-        _sampled_check(a, b, c, m, w.N, rng, n_entries=16,
-                       blocks=[(0, 128, 0, 256), (m - 128, m, w.N - 256, w.N)])
+    for c, ref in zip(dC, _reference(w)):
+        _full_check(c, ref)
     check_log(g, mode, [m // 128 for m in w.group_m], 16, 1, num_workers=148 if mode == "static" else None)
 
 
@@ -429,27 +527,6 @@ def test_randomized_shapes_and_modes(g):
             assert np.array_equal(C.astype(np.float64), ref), (i, M, N, K, tile, cl, mcast, mode)
     finally:
         g.set_opts(cluster_b_multicast=0, raster_group=16)
-
-
-@pytest.mark.parametrize("cl,mcast", [(2, 0), (2, 1), (4, 0), (C2X2, 0)],
-                         ids=["pair", "c2_shared_b", "c4_shared_b", "c2x2_shared_ab"])
-def test_square_full_size_cluster_modes(g, cl, mcast):
-    """The square workload in the cluster launch configurations the benchmark times beside
-    the headline (CLC): sampled elements and whole tiles against the oracle, exact log."""
-    w = wl.SQUARE
-    A, B = _inputs(w)
-    mt, nt, ncta, rn = grid_of(w.M, w.N, TILE_256, cl)
-    tm, tn = 128 * ncta // rn, 256 * rn   # cluster tile
-    g.set_opts(cluster_b_multicast=mcast)
-    try:
-        C = torch.full((w.M, w.N), float("nan"), device="cuda")
-        g.run(A.cuda(), B.cuda(), C, cluster=cl, sched="clc")
-        g.sync()
-        _sampled_check(A, B, C, w.M, w.N, np.random.default_rng(20 + ncta + rn + mcast),
-                       blocks=[(0, tm, 0, tn), (w.M - tm, w.M, w.N - tn, w.N)])
-        check_log(g, "clc", [mt], nt, ncta, rn=rn)
-    finally:
-        g.set_opts(cluster_b_multicast=0)
 
 
 @pytest.mark.parametrize("cl,mcast,mode", [(1, 0, "clc"), (1, 0, "static"), (2, 0, "clc"), (4, 0, "clc"),

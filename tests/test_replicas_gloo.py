@@ -27,6 +27,10 @@ def _worker(rank, ws, port, q):
         local_ms = [100.0, 125.0][rank]
         tflops, t = bench.job_throughput(local_ms, steps=10, flops_per_step=2e12, ws=ws)
         assert bench.dist_env() == (ws, rank, rank)
+        # the modes a replica times: no cluster shape that shares operands by TMA multicast
+        table = bench.mode_table(1, 256, 148, 152, bench.dist_env()[0])
+        assert table and not any(r["tma_multicast"] for r in table)
+        assert not any(r["sel"] == "clusters" for r in table)
         q.put((rank, t, tflops))
     finally:
         dist.destroy_process_group()
@@ -47,6 +51,18 @@ def test_two_replicas_take_the_slowest_time():
         assert t == 125.0
         # 2 replicas x 10 steps x 2 TFLOP in 125 ms
         assert tflops == pytest.approx(2 * 10 * 2.0 / 0.125)
+
+
+def test_mode_table_alone_keeps_the_cluster_rows():
+    """A process alone on its GPU (world size 1) also times the larger cluster shapes,
+    three of which share operands by TMA multicast; world size 2 drops all of them."""
+    import bench
+    alone = bench.mode_table(1, 256, 148, 152, 1)
+    assert sum(r["tma_multicast"] for r in alone) == 3
+    assert {r["key"] for r in alone if r["tma_multicast"]} == {
+        "clc_cluster2_shared_b", "clc_cluster4_shared_b", "clc_cluster2x2_shared_ab"}
+    two = bench.mode_table(1, 256, 148, 152, 2)
+    assert [r["key"] for r in two] == [r["key"] for r in alone if r["sel"] != "clusters"]
 
 
 def test_single_process_needs_no_group():

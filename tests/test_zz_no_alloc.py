@@ -3,17 +3,23 @@ whose device memory belongs to its own pool allocator or sits under a hard cap, 
 latency-critical path that cannot afford a cudaMalloc).  Its scratch is a fixed device
 array inside the library, shared by every call.
 
-Checked through the C ABI against gemm_run (the handle-based entry point) on two calls
-in a row, so the second call also shows that the scratch left behind by the first does
-not leak into its result.  Self-contained: it passes alone in a fresh process and after
-the other tests.  Collected last (file name) so a failure here cannot hide others.
+Checked through the C ABI on two calls in a row per case, against gemm_run (the
+handle-based entry point) within the tolerance the other tests use and against the CPU
+oracle, so the second call also shows that the scratch left behind by the first does not
+leak into its result; gemm_noalloc_status reads back each call's error word (zero) and
+ownership log (each tile computed once).  Self-contained: it passes alone in a fresh
+process and after the other tests.  Collected last (file name) so a failure here cannot
+hide others.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from oracle import within_tolerance
+from oracle import coverage as cv
+from tests.gpu_helpers import grid_of, linear_log
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +31,7 @@ def _reference(g, A, B, tile, cluster, sched):
     return C.cpu().numpy()
 
 
-def test_noalloc_matches_gemm_run_on_two_calls():
+def test_noalloc_matches_gemm_run_and_the_oracle_on_two_calls():
     import blackwell_clc_dynamic_gb300 as m
 
     cases = [
@@ -37,19 +43,32 @@ def test_noalloc_matches_gemm_run_on_two_calls():
     ]
     with m.Gemm(0) as g:
         for M, N, K, tile, cl, sched, seed in cases:
-            A = wl.make_matrix((M, K), seed).cuda()
-            B = wl.make_matrix((K, N), seed + 100).cuda()
+            A_h = wl.make_matrix((M, K), seed)
+            B_h = wl.make_matrix((K, N), seed + 100)
+            A, B = A_h.cuda(), B_h.cuda()
             ref = _reference(g, A, B, tile, cl, sched)
-            C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-            rc = m.gemm_run_noalloc(M, N, K, A, B, C, tile=tile, cluster=cl, sched=sched)
-            assert rc == m.GEMM_OK, m.gemm_strerror(rc)
-            torch.cuda.synchronize()
-            out = C.cpu().numpy()
-            ok, worst = within_tolerance(out, ref.astype(np.float64))
-            assert ok, f"gemm_run_noalloc differs from gemm_run: worst ratio {worst:.3g}"
+            exact = oracle.gemm(A_h, B_h)
+            mt, nt, ncta, rn = grid_of(M, N, tile, cl)
+            for call in range(2):
+                C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+                rc = m.gemm_run_noalloc(M, N, K, A, B, C, tile=tile, cluster=cl, sched=sched)
+                assert rc == m.GEMM_OK, m.gemm_strerror(rc)
+                # static launches one worker per SM (per cluster of SMs), the others one per tile
+                sms = torch.cuda.get_device_properties(0).multi_processor_count
+                n_workers = sms // ncta if sched == "static" else mt * nt
+                rc, words, owner, claims, first = m.gemm_noalloc_status(mt * nt * ncta, n_workers)
+                assert rc == m.GEMM_OK and words == (0, 0, 0), (rc, words)
+                out = C.cpu().numpy()
+                ok, worst = within_tolerance(out, ref.astype(np.float64))
+                assert ok, f"call {call}: gemm_run_noalloc differs from gemm_run: worst ratio {worst:.3g}"
+                ok, worst = within_tolerance(out, exact)
+                assert ok, f"call {call}: gemm_run_noalloc differs from the oracle: worst ratio {worst:.3g}"
+                owner_lin, claims_lin = linear_log(owner, claims, [mt], nt, ncta, group_rows=16, rn=rn)
+                cv.check_device_log(sched, owner_lin, claims_lin, first.tolist(), n_workers,
+                                    n_workers=n_workers if sched == "static" else None)
 
 
-def test_noalloc_rejects_problems_beyond_its_scratch():
+def test_noalloc_rejects_problems_beyond_its_scratch_and_host_memory():
     import blackwell_clc_dynamic_gb300 as m
 
     A = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
@@ -60,4 +79,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = m.gemm_run_noalloc(128 * 65537, 256, 64, A, B, C)
     assert rc == m.GEMM_ERR_SCRATCH_LIMIT
     assert "scratch" in m.gemm_strerror(rc)
+    # operands in pinned host memory: refused before any tensor map is made
+    C_host = torch.zeros((128, 256), dtype=torch.float32).pin_memory()
+    assert m.gemm_run_noalloc(128, 256, 64, A, B, C_host) == m.GEMM_ERR_INVALID_ARG
     torch.cuda.synchronize()
