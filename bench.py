@@ -63,9 +63,13 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="--impl reference: CPU seconds for all warm-up and timed steps together")
-    ap.add_argument("--settle-ms", type=float, default=1500.0,
-                    help="untimed back-to-back launches before the first timed mode, so every mode is timed "
-                         "at the same power and clock state")
+    ap.add_argument("--settle-ms", type=float, default=0.0,
+                    help="untimed back-to-back launches before the first timed mode (a sustained power state)")
+    ap.add_argument("--clock-extend-ms", type=float, default=400.0,
+                    help="untimed launches after the timed CLC region while the clock sampler runs")
+    ap.add_argument("--cooldown-ms", type=float, default=300.0,
+                    help="idle time before every timed mode, so each mode (CLC first) starts from the same "
+                         "power and clock state")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--all-out", default="bench_all.json", help="where --all writes its JSON")
     ap.add_argument("--all-steps", type=int, default=60)
@@ -138,7 +142,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device: int):
+    def __init__(self, device: int, interval_ms: int = 200):
+        self.interval_ms = interval_ms
         self.sel = None
         try:
             import torch
@@ -152,7 +157,8 @@ class ClockSampler:
         self.proc = None
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+               str(self.interval_ms)]
         if self.sel:
             cmd += ["-i", self.sel]
         try:
@@ -387,7 +393,7 @@ def run_ours(args, ws, rank, local):
         g.occupy_start(args.occupy, limit_ns=120_000_000_000, stream=s_occ)
         g.occupy_wait_resident(10_000)
 
-    # settle: the first timed mode would otherwise run on a cooler, faster-clocked GPU
+    # optional settle into a sustained power state before the first mode (--settle-ms)
     t_end = time.perf_counter() + args.settle_ms / 1e3
     settle = step("clc")
     while time.perf_counter() < t_end:
@@ -403,12 +409,25 @@ def run_ours(args, ws, rank, local):
         for r in order:
             key, mode, nw, ccl, mcast, pdl = r["key"], r["sched"], r["nw"], r["cl"], r["mcast"], r["pdl"]
             g.set_opts(cluster_b_multicast=mcast, pdl=pdl, log_enable=r["log"])
-            sampler = ClockSampler(local) if key == "clc" else None
+            # every mode starts from the same idle state: under the 1.4 kW power cap the clock
+            # a mode runs at depends on how long the GPU has been busy before it
+            sync_all()
+            time.sleep(args.cooldown_ms / 1e3)
+            sampler = ClockSampler(local, interval_ms=50) if key == "clc" else None
             if sampler:
                 sampler.start()
             total_ms, per = time_steps(step(mode, nw, ccl), args.steps, args.warmup, stream, barrier, sync_all)
             if sampler:
+                # a timed region of a few tens of milliseconds may hold no sample: the same
+                # launches continue, untimed, until the sampler has seen the load
+                fn, t_ext = step(mode, nw, ccl), time.perf_counter() + args.clock_extend_ms / 1e3
+                while time.perf_counter() < t_ext:
+                    for _ in range(20):
+                        fn()
+                    sync_all()
                 clocks = sampler.stop()
+                clocks["window"] = (f"warm-up + {args.steps} timed launches + {args.clock_extend_ms:.0f} ms of the "
+                                    f"same launches untimed; nvidia-smi every 50 ms")
             tflops, total_ms = job_throughput(total_ms, args.steps, w.flops, ws)
             modes[key] = {"tflops": tflops, "ms_per_step": total_ms / args.steps,
                           "ms_min": min(per), "ms_median": statistics.median(per), "ms_max": max(per),
@@ -606,6 +625,8 @@ def workload_rows(g, args, peaks, sms):
     out = {}
 
     def timed(label, fn, flops, min_bytes, extra=None):
+        st.synchronize()
+        time.sleep(args.cooldown_ms / 1e3)   # the same idle state before every loop
         sampler = ClockSampler(torch.cuda.current_device())
         sampler.start()
         try:
