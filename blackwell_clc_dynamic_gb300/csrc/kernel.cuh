@@ -10,6 +10,8 @@
 //               16-byte responses, bounded by a throttle pipeline
 //   warp 3      spare
 //   warps 4..7  epilogue: TMEM -> registers -> swizzled shared memory -> TMA store of fp32 C
+//               (a CTA's last tile is staged whole in the idle operand ring, without
+//               waiting for one store to release a buffer before the next)
 //
 // The schedule (what the "CUTLASS CLC dynamic persistent kernel" page calls the three kinds
 // of kernel, section "From one tile per block to one worker working continuously"):
@@ -140,6 +142,11 @@ struct Cfg {
   static constexpr int C_ROW = EPI_CHUNK * 4;                  // bytes per staged C row (64 or 128)
   static constexpr int C_BUFS = FINE ? 1 : 2;                  // staging buffers per epilogue warp
   static constexpr int C_BUF_BYTES = 32 * C_ROW;
+  // A CTA's last tile: the operand ring is idle, so each epilogue warp stages its whole 32
+  // rows there (one buffer per chunk).  Not in the multicast clusters, whose rings peer
+  // CTAs also write.
+  static constexpr bool RING_STAGING = !MCAST;
+  static constexpr int CHUNKS = BN / EPI_CHUNK;                // stores per epilogue warp per tile
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
@@ -163,6 +170,7 @@ struct Cfg {
   static_assert(B_BOXES % (MCAST ? RM : 1) == 0, "B boxes split evenly over a cluster column");
   static_assert((A_OWN_ROWS * A_ROW) % 1024 == 0, "A halves start on a swizzle atom");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && C_BUF_BYTES % 1024 == 0, "1 KiB alignment");
+  static_assert(!RING_STAGING || 4 * CHUNKS * C_BUF_BYTES <= STAGES * (A_BYTES + B_BYTES), "last tile fits the ring");
 };
 
 // Host view of a shape's TMA boxes and k-slice depth.
@@ -654,8 +662,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const uint32_t acc_empty_leader0 = PAIR ? map_to_rank(bar(C::BAR_ACC_EMPTY), 0) : bar(C::BAR_ACC_EMPTY);
     int chunk_seq = 0;
     while (w.valid) {
+      // The tile after this one, taken before this one is drained (its response was fetched
+      // a tile ago): none means this is the CTA's last tile.  A wait that runs out here
+      // still lets the current tile be drained: its accumulator completes on its own.
+      const Work nxt = it.next(p, rank, sb, ctl, true);
       if (kBoundsCheck && w.skip) {
-        w = it.next(p, rank, sb, ctl, true);
+        w = nxt;
         continue;
       }
       if (!bar_wait(bar(C::BAR_ACC_FULL + acc), aph, p, ctl, WAIT_ACC_FULL)) break;
@@ -663,6 +675,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       if (p.trace && q == 0 && lane == 0) p.trace[TRACE_WORDS * (size_t)w.pos + 6] = globaltimer();
       const CUtensorMap* mC = p.G ? p.gmaps + 3 * w.g + 2 : &p.tmC;
       const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      // Last tile: the producer has issued its final load and the accumulator is complete, so
+      // every MMA that read the ring has finished and the whole ring is free.
+      const bool ring_stage = C::RING_STAGING && !nxt.valid;
+      if (ring_stage) fence_proxy_async_smem();   // the ring was last written by TMA loads
 #pragma unroll 1
       for (int ch = 0; ch < BN / C::EPI_CHUNK; ++ch) {
         uint32_t v[C::EPI_CHUNK];
@@ -682,9 +698,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < C::EPI_CHUNK; ++j) v[j] = 0u;
         }
-        const uint32_t buf = cbuf + (uint32_t)(chunk_seq % C::C_BUFS) * C::C_BUF_BYTES;
-        // the store that last used `buf` has finished reading it
-        if (lane == 0) bulk_wait_group_read<C::C_BUFS - 1>();
+        const uint32_t buf = ring_stage ? sb + C::OFF_A + (uint32_t)(q * C::CHUNKS + ch) * C::C_BUF_BYTES
+                                        : cbuf + (uint32_t)(chunk_seq % C::C_BUFS) * C::C_BUF_BYTES;
+        // the store that last used `buf` has finished reading it (a ring buffer is used once)
+        if (!ring_stage && lane == 0) bulk_wait_group_read<C::C_BUFS - 1>();
         __syncwarp();
         // row `lane` of the box; TMA swizzle: 16-byte chunk j of a 128-byte row sits at
         // j ^ (row % 8), of a 64-byte row at j ^ ((row / 2) % 4)
@@ -723,7 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       first_tile = false;
       acc ^= 1;
       if (acc == 0) aph ^= 1;
-      w = it.next(p, rank, sb, ctl, true);
+      w = nxt;
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
