@@ -66,6 +66,9 @@ def test_noalloc_matches_gemm_run_and_the_oracle_on_two_calls():
                 owner_lin, claims_lin = linear_log(owner, claims, [mt], nt, ncta, group_rows=16, rn=rn)
                 cv.check_device_log(sched, owner_lin, claims_lin, first.tolist(), n_workers,
                                     n_workers=n_workers if sched == "static" else None)
+                # the log's sizes must be the latest call's
+                rc, *_ = m.gemm_noalloc_status(mt * nt * ncta + 1, n_workers)
+                assert rc == m.GEMM_ERR_INVALID_ARG
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch_and_host_memory():
