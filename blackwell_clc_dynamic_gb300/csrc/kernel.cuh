@@ -676,8 +676,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       const CUtensorMap* mC = p.G ? p.gmaps + 3 * w.g + 2 : &p.tmC;
       const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       // Last tile: the producer has issued its final load and the accumulator is complete, so
-      // every MMA that read the ring has finished and the whole ring is free.
-      const bool ring_stage = C::RING_STAGING && !nxt.valid;
+      // every MMA that read the ring has finished and the whole ring is free.  Not after a
+      // wait of this CTA ran out: then "no next tile" may be this warp's own timeout, and
+      // the ring is left alone.
+      const bool ring_stage = C::RING_STAGING && !nxt.valid && *ctl.abort == 0;
       if (ring_stage) fence_proxy_async_smem();   // the ring was last written by TMA loads
 #pragma unroll 1
       for (int ch = 0; ch < BN / C::EPI_CHUNK; ++ch) {
