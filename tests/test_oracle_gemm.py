@@ -168,3 +168,15 @@ def test_transpose_identity_bit_exact():
     At = torch.from_numpy(A.view(np.int16)).t().contiguous().view(torch.bfloat16)
     Bt = torch.from_numpy(B.view(np.int16)).t().contiguous().view(torch.bfloat16)
     assert np.array_equal(oracle.gemm(Bt, At), C.T)
+
+
+def test_depth_scaled_tolerance_rule():
+    """The acceptance rule for products deeper than the stated workloads: the stated 1e-3
+    up to K = 8192, then scaled by (K / 8192)^1.5 (the growth of the tensor cores'
+    accumulation error bound); monotone, and exactly the stated value at the stated depths."""
+    from tests.gpu_helpers import rel_tolerance
+    assert rel_tolerance(0) == rel_tolerance(1000) == rel_tolerance(8192) == 1e-3
+    assert abs(rel_tolerance(16384) - 1e-3 * 2 ** 1.5) < 1e-15
+    assert abs(rel_tolerance(12800) - 1e-3 * (12800 / 8192) ** 1.5) < 1e-15
+    ks = [8192, 9000, 10752, 12544, 12800, 16384]
+    assert all(rel_tolerance(a) < rel_tolerance(b) for a, b in zip(ks, ks[1:]))
