@@ -532,11 +532,10 @@ def test_randomized_shapes_and_modes(g):
     """24 seeded random problems: ragged M, N, K (multiples of 8 where the ABI needs it),
     every schedule and cluster shape, integer inputs so the result must be bit-exact."""
     rng = np.random.default_rng(2024)
-    configs = list(SHAPES)
     try:
         for i in range(24):
-            tile, cl, mcast = configs[i % len(configs)]
-            mode = MODES[(i // len(configs)) % 3]
+            tile, cl, mcast = SHAPES[i % len(SHAPES)]
+            mode = MODES[(i // len(SHAPES)) % 3]
             M = int(rng.integers(1, 1500))
             N = 8 * int(rng.integers(1, 160))
             K = 8 * int(rng.integers(0, 200))
