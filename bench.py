@@ -525,6 +525,13 @@ def run_ours(args, ws, rank, local):
                      "tensor_frac_burst": achieved / peaks["bf16_tflops"]})
     roof["arithmetic_intensity"] = ai
     roof["ridge_flop_per_byte"] = ridge
+    if not grouped and cl == 1:
+        # operand bytes every tile streams from L2 into shared memory (A's 128 x K rows and
+        # B's K x 256 columns, bf16), the bound of the one-CTA shape; per launch and per second
+        tm, tn = -(-w.M // 128), -(-w.N // w.bn)
+        stream = tm * tn * (128 * w.K + w.K * w.bn) * 2.0
+        roof["l2_to_smem_operand_bytes_per_launch"] = stream
+        roof["l2_to_smem_operand_tbs"] = stream / (kernel_ms * 1e-3) / 1e12
     if clocks and clocks.get("sm_mhz"):
         # the tensor pipe's own bound at the clock the SMs actually ran: 8192 dense bf16 flop
         # per SM clock (one 128 x 256 x 16 MMA per 128 clocks), times the SMs, times the
