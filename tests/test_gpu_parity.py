@@ -130,6 +130,24 @@ def test_argument_errors(g):
     assert m.gemm_run(h, 128, 256, 64, None, B, C) == m.GEMM_ERR_INVALID_ARG
 
 
+def test_size_limits_and_empty_calls(g):
+    """Sizes beyond 32-bit tile and row counts are refused before anything is allocated or
+    launched; an empty grouped call and zero-sized problems are no-ops."""
+    import blackwell_clc_dynamic_gb300 as m
+    A = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((128, 256), dtype=torch.float32, device="cuda")
+    h = g.h
+    assert m.gemm_run(h, 1 << 31, 256, 64, A, B, C) == m.GEMM_ERR_TOO_LARGE
+    assert m.gemm_run(h, 128, 1 << 31, 64, A, B, C) == m.GEMM_ERR_TOO_LARGE
+    assert m.gemm_run(h, 128, 256, 1 << 31, A, B, C) == m.GEMM_ERR_TOO_LARGE
+    assert m.gemm_run_grouped(h, [], 256, 64, [], [], []) == m.GEMM_OK
+    assert m.gemm_run_grouped_v(h, [0, 0], [256, 256], [64, 64], [A, A], [B, B], [C, C]) == m.GEMM_OK
+    assert m.gemm_run(h, 0, 256, 64, A, B, C) == m.GEMM_OK
+    assert m.gemm_run(h, 128, 0, 64, A, B, C) == m.GEMM_OK
+    g.sync()
+
+
 def test_operands_must_be_memory_of_the_handles_device(g):
     """A, B and C must be device memory of the handle's GPU: pinned host memory (which the
     GPU could reach) is refused before any tensor map is encoded, for every entry point."""
