@@ -679,7 +679,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       // every MMA that read the ring has finished and the whole ring is free.  Not after a
       // wait of this CTA ran out: then "no next tile" may be this warp's own timeout, and
       // the ring is left alone.
-      const bool ring_stage = C::RING_STAGING && !nxt.valid && *ctl.abort == 0;
+      // (Decided by lane 0 for the whole warp: the flag may change while lanes read it.)
+      const bool ring_stage =
+          __shfl_sync(0xffffffffu, (int)(C::RING_STAGING && !nxt.valid && *ctl.abort == 0), 0) != 0;
       if (ring_stage) fence_proxy_async_smem();   // the ring was last written by TMA loads
 #pragma unroll 1
       for (int ch = 0; ch < BN / C::EPI_CHUNK; ++ch) {
